@@ -1,0 +1,309 @@
+// bwd_dq.cu -- first kernel of the atomic-free split backward ("backward
+// query" of the metal-flash-attention page's pseudocode): one CTA per 128-row
+// query tile of one (batch, head), iterating over K/V tiles.
+//
+//   D_i = sum_d dO_id O_id                          (prologue, written out)
+//   per K/V tile j:  S = Q K_j^T,  P = exp(S scale - L)  (base 2 here),
+//                    dP = dO V_j^T,  dS = P * (dP - D) * scale,
+//                    dQ += dS K_j
+//   dQ written once after the last tile.  Three GEMMs per tile; no atomics and
+//   no scratch: each CTA owns its dQ rows outright (the design the page adopts
+//   because float atomics are emulated on its GPU; it parallelises fully over
+//   query rows here as there).
+//
+// GB300 mapping: warp 0 TMA producer (Q and dO once; K_j, V_j through a ring),
+// warp 1 TMEM allocator + tcgen05 issuer, warps 2-5 one query row per thread.
+// TMEM: S [0,128), dP [128,256), dQ [256, 256+D), dS [256+D, 320+D).  dS
+// (bf16) is fed to the dQ MMA straight from TMEM (A operand); K_j is the B
+// operand in MN-major form (keys are the reduction).  MMAs on different
+// accumulators are not ordered with each other, so dS has its own columns:
+// the compute warps write dS_j only after S_j / dP_j completed, and the commit
+// behind those tracks dQ_{j-1}, the previous reader of the dS buffer.
+#include "fa_internal.h"
+#include "sm100_ptx.cuh"
+#include <cmath>
+
+namespace fa {
+namespace {
+
+constexpr int kBM = 128, kBN = 128;
+constexpr int kThreads = 192;
+
+enum : int { kSiteQ = 21, kSiteSlotEmpty, kSiteSlotFull, kSiteSFull, kSiteDsFull, kSiteDq, kSiteFinal, kSiteDrain };
+
+template <int D, int NSLOT>
+struct DqSmem {
+    static constexpr int kTileBytes = kBM * D * 2;  // Q, dO, K_j, V_j tiles are all 128 x D bf16
+    static constexpr int kQOff = 0;
+    static constexpr int kDoOff = kTileBytes;
+    static constexpr int kSlotOff = 2 * kTileBytes;
+    static constexpr int kBarOff = kSlotOff + NSLOT * kTileBytes;
+    // q_full, slot_full[NSLOT], slot_empty[NSLOT], s_full, ds_full, dq_done, final
+    static constexpr int kNumBars = 1 + 2 * NSLOT + 4;
+    static constexpr int kTmemHolderOff = kBarOff + kNumBars * 8;
+    static constexpr int kAlloc = kTmemHolderOff + 16 + 1024;
+};
+
+template <int D, int NSLOT>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                  const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
+                  BwdArgs a) {
+    using L = DqSmem<D, NSLOT>;
+    constexpr int kPanels = D / 64;
+    constexpr uint32_t kTmemCols = 512;
+    constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 256 + D;
+    static_assert(kColDS + 64 <= 512, "TMEM budget");
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *q_s = smem + L::kQOff;
+    uint8_t *do_s = smem + L::kDoOff;
+    uint8_t *slots = smem + L::kSlotOff;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
+    uint64_t *q_full = bars;
+    uint64_t *slot_full = bars + 1;
+    uint64_t *slot_empty = slot_full + NSLOT;
+    uint64_t *s_full = slot_empty + NSLOT;  // S and dP of the tile are both ready
+    uint64_t *ds_full = s_full + 1;
+    uint64_t *dq_done = ds_full + 1;
+    uint64_t *final_bar = dq_done + 1;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kTmemHolderOff);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q_tile = gridDim.x - 1 - blockIdx.x;
+    const int bh = blockIdx.z * a.H + blockIdx.y;
+    const int N = a.N;
+    const int kv_end = a.causal ? min(N, (q_tile + 1) * kBM) : N;
+    const int n_kv = (kv_end + kBN - 1) / kBN;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < NSLOT; ++s) {
+            mbar_init(&slot_full[s], 1);
+            mbar_init(&slot_empty[s], 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(ds_full, 128);
+        mbar_init(dq_done, 1);
+        mbar_init(final_bar, 1);
+        fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tmap_q);
+            tma_prefetch_desc(&tmap_k);
+            tma_prefetch_desc(&tmap_v);
+            tma_prefetch_desc(&tmap_do);
+            mbar_arrive_expect_tx(q_full, 2 * L::kTileBytes);
+#pragma unroll
+            for (int p = 0; p < kPanels; ++p) {
+                tma_load_3d(q_s + p * (kBM * 128), &tmap_q, q_full, p * 64, q_tile * kBM, bh);
+                tma_load_3d(do_s + p * (kBM * 128), &tmap_do, q_full, p * 64, q_tile * kBM, bh);
+            }
+            int last_round[NSLOT];
+#pragma unroll
+            for (int s = 0; s < NSLOT; ++s) last_round[s] = -1;
+            for (int idx = 0; idx < 2 * n_kv; ++idx) {
+                const int slot = idx % NSLOT, round = idx / NSLOT;
+                if (!mbar_wait(&slot_empty[slot], (round & 1) ^ 1, a.status, kSiteSlotEmpty)) break;
+                uint8_t *dst = slots + slot * L::kTileBytes;
+                const CUtensorMap *map = (idx & 1) ? &tmap_v : &tmap_k;
+                mbar_arrive_expect_tx(&slot_full[slot], L::kTileBytes);
+#pragma unroll
+                for (int p = 0; p < kPanels; ++p)
+                    tma_load_3d(dst + p * (kBN * 128), map, &slot_full[slot], p * 64, (idx >> 1) * kBN, bh);
+#pragma unroll
+                for (int s = 0; s < NSLOT; ++s)
+                    if (s == slot) last_round[s] = round;
+            }
+#pragma unroll
+            for (int s = 0; s < NSLOT; ++s)
+                if (last_round[s] >= 0) mbar_wait(&slot_full[s], last_round[s] & 1, a.status, kSiteDrain);
+            mbar_wait(q_full, 0, a.status, kSiteDrain);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc_sq = idesc_bf16_f32(kBM, kBN, false, false);  // S, dP
+            constexpr uint32_t idesc_dq = idesc_bf16_f32(kBM, D, false, true);     // dQ += dS K
+            const uint32_t q_addr = smem_u32(q_s), do_addr = smem_u32(do_s), slot_addr = smem_u32(slots);
+            bool ok = mbar_wait(q_full, 0, a.status, kSiteQ);
+            tc_fence_after();
+            for (int j = 0; ok && j < n_kv; ++j) {
+                const int ks_idx = 2 * j, k_slot = ks_idx % NSLOT, k_round = ks_idx / NSLOT;
+                const int vs_idx = 2 * j + 1, v_slot = vs_idx % NSLOT, v_round = vs_idx / NSLOT;
+                if (!(ok = mbar_wait(&slot_full[k_slot], k_round & 1, a.status, kSiteSlotFull))) break;
+                if (!(ok = mbar_wait(&slot_full[v_slot], v_round & 1, a.status, kSiteSlotFull))) break;
+                tc_fence_after();
+                const uint32_t kbase = slot_addr + k_slot * L::kTileBytes;
+                const uint32_t vbase = slot_addr + v_slot * L::kTileBytes;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks >> 2) * (kBM * 128) + (ks & 3) * 32;
+                    mma_ss(tmem + kColS, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
+                           idesc_sq, ks > 0);
+                }
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks >> 2) * (kBM * 128) + (ks & 3) * 32;
+                    mma_ss(tmem + kColDP, sdesc_sw128(do_addr + off, 16, 1024), sdesc_sw128(vbase + off, 16, 1024),
+                           idesc_sq, ks > 0);
+                }
+                mma_commit(s_full);
+                mma_commit(&slot_empty[v_slot]);
+                if (!(ok = mbar_wait(ds_full, j & 1, a.status, kSiteDsFull))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    mma_ts(tmem + kColDQ, tmem + kColDS + kk * 8, sdesc_sw128(kbase + kk * 2048, kBN * 128, 1024),
+                           idesc_dq, (j > 0 || kk > 0));
+                mma_commit(&slot_empty[k_slot]);
+                mma_commit(dq_done);
+            }
+            mma_commit(final_bar);
+            mbar_wait(final_bar, 0, a.status, kSiteFinal);
+        }
+        __syncwarp();
+    } else {
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const int row = q_tile * kBM + r;
+        const bool valid = row < N;
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const float c = a.scale_log2;
+        // D_i = sum_d dO_id O_id for this thread's row.
+        float delta = 0.f;
+        if (valid) {
+            const uint4 *orow = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.o) +
+                                                                ((size_t)bh * N + row) * D);
+            const uint4 *drow = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.dO) +
+                                                                ((size_t)bh * N + row) * D);
+#pragma unroll 4
+            for (int i = 0; i < D / 8; ++i) {
+                const uint4 ov = orow[i], dv = drow[i];
+                const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, dw[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ow[t]));
+                    const float2 df = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&dw[t]));
+                    delta = fmaf(of.x, df.x, delta);
+                    delta = fmaf(of.y, df.y, delta);
+                }
+            }
+            a.delta[(size_t)bh * N + row] = delta;
+        }
+        // P = 2^(S c - L log2 e); invalid rows get P = 0.
+        const float lse2 = valid ? a.lse[(size_t)bh * N + row] * 1.4426950408889634f : INFINITY;
+        const float sc = a.scale;
+        bool ok = true;
+        for (int j = 0; j < n_kv; ++j) {
+            ok = mbar_wait(s_full, j & 1, a.status, kSiteSFull);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            tc_fence_after();
+            const int key0 = j * kBN;
+            const bool need_mask = (key0 + kBN > N) || (a.causal && key0 + kBN - 1 > q_tile * kBM);
+            const int lim = a.causal ? min(N - 1, row) : N - 1;
+#pragma unroll
+            for (int ch = 0; ch < kBN / 32; ++ch) {
+                uint32_t sraw[32], praw[32], dsk[16];
+                tmem_ld32(tmem + lane_base + kColS + ch * 32, sraw);
+                tmem_ld32(tmem + lane_base + kColDP + ch * 32, praw);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    float p0 = ex2_approx(fmaf(__uint_as_float(sraw[i]), c, -lse2));
+                    float p1 = ex2_approx(fmaf(__uint_as_float(sraw[i + 1]), c, -lse2));
+                    if (need_mask) {
+                        if (key0 + ch * 32 + i > lim) p0 = 0.f;
+                        if (key0 + ch * 32 + i + 1 > lim) p1 = 0.f;
+                    }
+                    const float ds0 = p0 * (__uint_as_float(praw[i]) - delta) * sc;
+                    const float ds1 = p1 * (__uint_as_float(praw[i + 1]) - delta) * sc;
+                    dsk[i / 2] = pack_bf16x2(ds0, ds1);
+                }
+                tmem_st16(tmem + lane_base + kColDS + ch * 16, dsk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(ds_full);
+        }
+        if (ok) {
+            ok = mbar_wait(dq_done, (n_kv - 1) & 1, a.status, kSiteDq);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        if (ok) {
+            tc_fence_after();
+            uint32_t v[32];
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch) {
+                tmem_ld32(tmem + lane_base + kColDQ + ch * 32, v);
+                tmem_wait_ld();
+                if (valid) {
+                    if (a.grad_bf16) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.dq) +
+                                                               ((size_t)bh * N + row) * D + ch * 32);
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(v[v4 * 8 + 0]), __uint_as_float(v[v4 * 8 + 1]));
+                            w.y = pack_bf16x2(__uint_as_float(v[v4 * 8 + 2]), __uint_as_float(v[v4 * 8 + 3]));
+                            w.z = pack_bf16x2(__uint_as_float(v[v4 * 8 + 4]), __uint_as_float(v[v4 * 8 + 5]));
+                            w.w = pack_bf16x2(__uint_as_float(v[v4 * 8 + 6]), __uint_as_float(v[v4 * 8 + 7]));
+                            dst[v4] = w;
+                        }
+                    } else {
+                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.dq) +
+                                                                 ((size_t)bh * N + row) * D + ch * 32);
+#pragma unroll
+                        for (int v4 = 0; v4 < 8; ++v4)
+                            dst[v4] = make_float4(__uint_as_float(v[v4 * 4 + 0]), __uint_as_float(v[v4 * 4 + 1]),
+                                                  __uint_as_float(v[v4 * 4 + 2]), __uint_as_float(v[v4 * 4 + 3]));
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int D, int NSLOT>
+cudaError_t launch_spec(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                        const CUtensorMap &tdo, cudaStream_t s) {
+    using L = DqSmem<D, NSLOT>;
+    static_assert(L::kAlloc <= 232448, "shared memory budget");
+    auto kern = bwd_dq_kernel<D, NSLOT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    if (e != cudaSuccess) return e;
+    dim3 grid((a.N + kBM - 1) / kBM, a.H, a.B);
+    kern<<<grid, kThreads, L::kAlloc, s>>>(tq, tk, tv, tdo, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_dq(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                          const CUtensorMap &tdo, cudaStream_t s) {
+    switch (a.D) {
+        case 64: return launch_spec<64, 8>(a, tq, tk, tv, tdo, s);
+        case 128: return launch_spec<128, 4>(a, tq, tk, tv, tdo, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace fa

@@ -1,0 +1,271 @@
+// fa_api.cu -- the C ABI declared in include/fa.h: argument validation,
+// TMA descriptor encoding, and launches on the caller's stream.
+//
+// Nothing here allocates device memory.  The only device-side state is the
+// status word below (one int per device in the library's own static storage),
+// which kernels update when a bounded wait runs out.
+#include "../../include/fa.h"
+#include "fa_internal.h"
+#include "sm100_ptx.cuh"
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+namespace fa {
+
+__device__ int g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    int status_code = 0;  // FA_OK or the fa_status of the failed set-up
+    int *status_word = nullptr;
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Per-device set-up: architecture check and the status word's device address.
+int device_state(int *dev_out, DeviceState **st_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_DEVICE;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState &st = g_dev[dev];
+    if (!st.ready) {
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return FA_ERR_CUDA;
+        if (!(prop.major == 10 && prop.minor == 3)) {
+            st.status_code = FA_ERR_DEVICE;  // kernels are built for sm_103a only
+        } else if (cudaGetSymbolAddress(reinterpret_cast<void **>(&st.status_word), g_status_word) != cudaSuccess) {
+            st.status_code = FA_ERR_CUDA;
+        } else {
+            st.status_code = FA_OK;
+        }
+        if (!g_encode && st.status_code == FA_OK) {
+            cudaDriverEntryPointQueryResult q;
+            void *fn = nullptr;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                    cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || !fn)
+                st.status_code = FA_ERR_CUDA;
+            else
+                g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        }
+        st.ready = true;
+    }
+    *dev_out = dev;
+    *st_out = &st;
+    return st.status_code;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Device-accessible (device or managed memory on the current device).
+int check_device_ptr(const void *p) {
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_DEVICE_PTR;
+    }
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) return FA_ERR_DEVICE_PTR;
+    return FA_OK;
+}
+
+int check_ptrs(std::initializer_list<const void *> ptrs) {
+    for (const void *p : ptrs)
+        if (!p) return FA_ERR_NULL;
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return FA_ERR_ALIGN;
+    for (const void *p : ptrs) {
+        int rc = check_device_ptr(p);
+        if (rc != FA_OK) return rc;
+    }
+    return FA_OK;
+}
+
+int check_shape(int B, int H, int N, int D, float scale) {
+    if (B < 1 || H < 1 || N < 1 || D < 1) return FA_ERR_SHAPE;
+    if (B > 65535 || H > 65535) return FA_ERR_SHAPE;  // grid y / z limits
+    if ((long long)B * H * (long long)N > (1ll << 31) - 1) return FA_ERR_SHAPE;
+    if (!std::isfinite(scale)) return FA_ERR_SCALE;
+    return FA_OK;
+}
+
+// [B*H, N, D] bf16 tensor, box {64, rows, 1}, 128-byte swizzle, zero fill out of bounds.
+int encode_bf16_3d(CUtensorMap *map, const void *base, int BH, int N, int D, int box_rows) {
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+float log2e() { return 1.4426950408889634f; }
+
+}  // namespace
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" int fa_forward(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N,
+                          int D, float scale, int causal, int dtype, void *stream) {
+    int rc = check_shape(B, H, N, D, scale);
+    if (rc != FA_OK) return rc;
+    if (dtype == FA_BF16) {
+        if (D != 64 && D != 128 && D != 256) return FA_ERR_HEAD_DIM;
+    } else if (dtype == FA_F32) {
+        if (D % 32 != 0 || D > 256) return FA_ERR_HEAD_DIM;
+    } else {
+        return FA_ERR_DTYPE;
+    }
+    rc = check_ptrs({q, k, v, o, lse});
+    if (rc != FA_OK) return rc;
+    int dev;
+    DeviceState *st;
+    rc = device_state(&dev, &st);
+    if (rc != FA_OK) return rc;
+
+    FwdArgs a{q, k, v, o, lse, B, H, N, D, scale, scale * log2e(), causal ? 1 : 0, st->status_word};
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (dtype == FA_F32) {
+        e = launch_fwd_f32(a, s);
+    } else {
+        CUtensorMap tq, tk, tv;
+        const int bn = fwd_block_n(D);
+        if (encode_bf16_3d(&tq, q, B * H, N, D, 128) != FA_OK || encode_bf16_3d(&tk, k, B * H, N, D, bn) != FA_OK ||
+            encode_bf16_3d(&tv, v, B * H, N, D, bn) != FA_OK)
+            return FA_ERR_CUDA;
+        e = launch_fwd_bf16(a, tq, tk, tv, s);
+    }
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+extern "C" int fa_backward_dq(const void *q, const void *k, const void *v, const void *o, const void *dO,
+                              const float *lse, float *delta, void *dq, int B, int H, int N, int D, float scale,
+                              int causal, int dtype, int grad_dtype, void *stream) {
+    int rc = check_shape(B, H, N, D, scale);
+    if (rc != FA_OK) return rc;
+    if (dtype != FA_BF16 && dtype != FA_F32) return FA_ERR_DTYPE;
+    if (grad_dtype != FA_BF16 && grad_dtype != FA_F32) return FA_ERR_DTYPE;
+    if (dtype != FA_BF16) return FA_ERR_DTYPE;  // the split backward runs on bf16 inputs
+    if (D != 64 && D != 128) return FA_ERR_HEAD_DIM;
+    rc = check_ptrs({q, k, v, o, dO, lse, delta, dq});
+    if (rc != FA_OK) return rc;
+    int dev;
+    DeviceState *st;
+    rc = device_state(&dev, &st);
+    if (rc != FA_OK) return rc;
+    BwdArgs a{q, k, v, o, dO, lse, delta, dq, nullptr, nullptr, B, H, N, D, scale, scale * log2e(),
+              causal ? 1 : 0, grad_dtype == FA_BF16 ? 1 : 0, st->status_word};
+    CUtensorMap tq, tk, tv, tdo;
+    if (encode_bf16_3d(&tq, q, B * H, N, D, 128) != FA_OK || encode_bf16_3d(&tk, k, B * H, N, D, 128) != FA_OK ||
+        encode_bf16_3d(&tv, v, B * H, N, D, 128) != FA_OK || encode_bf16_3d(&tdo, dO, B * H, N, D, 128) != FA_OK)
+        return FA_ERR_CUDA;
+    cudaError_t e = launch_bwd_dq(a, tq, tk, tv, tdo, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+extern "C" int fa_backward_dkdv(const void *q, const void *k, const void *v, const void *dO, const float *lse,
+                                const float *delta, void *dk, void *dv, int B, int H, int N, int D, float scale,
+                                int causal, int dtype, int grad_dtype, void *stream) {
+    int rc = check_shape(B, H, N, D, scale);
+    if (rc != FA_OK) return rc;
+    if (dtype != FA_BF16 && dtype != FA_F32) return FA_ERR_DTYPE;
+    if (grad_dtype != FA_BF16 && grad_dtype != FA_F32) return FA_ERR_DTYPE;
+    if (dtype != FA_BF16) return FA_ERR_DTYPE;
+    if (D != 64 && D != 128) return FA_ERR_HEAD_DIM;
+    rc = check_ptrs({q, k, v, dO, lse, delta, dk, dv});
+    if (rc != FA_OK) return rc;
+    int dev;
+    DeviceState *st;
+    rc = device_state(&dev, &st);
+    if (rc != FA_OK) return rc;
+    BwdArgs a{q, k, v, nullptr, dO, lse, const_cast<float *>(delta), nullptr, dk, dv, B, H, N, D, scale,
+              scale * log2e(), causal ? 1 : 0, grad_dtype == FA_BF16 ? 1 : 0, st->status_word};
+    CUtensorMap tq, tk, tv, tdo;
+    if (encode_bf16_3d(&tq, q, B * H, N, D, 128) != FA_OK || encode_bf16_3d(&tk, k, B * H, N, D, 128) != FA_OK ||
+        encode_bf16_3d(&tv, v, B * H, N, D, 128) != FA_OK || encode_bf16_3d(&tdo, dO, B * H, N, D, 128) != FA_OK)
+        return FA_ERR_CUDA;
+    cudaError_t e = launch_bwd_dkdv(a, tq, tk, tv, tdo, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+extern "C" const char *fa_status_string(int status) {
+    switch (status) {
+        case FA_OK: return "ok";
+        case FA_ERR_NULL: return "a required pointer is NULL";
+        case FA_ERR_SHAPE: return "invalid shape (B, H, N must be >= 1 and within index limits)";
+        case FA_ERR_HEAD_DIM: return "head dimension not supported for this dtype / pass";
+        case FA_ERR_DTYPE: return "unsupported dtype or grad_dtype";
+        case FA_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case FA_ERR_SCALE: return "scale is not finite";
+        case FA_ERR_CUDA: return "CUDA runtime error";
+        case FA_ERR_TIMEOUT: return "a bounded in-kernel wait ran out";
+        case FA_ERR_DEVICE_PTR: return "pointer is not device-accessible memory";
+        case FA_ERR_DEVICE: return "current device is not sm_103 (GB300)";
+        default: return "unknown status";
+    }
+}
+
+extern "C" int fa_device_status(void *stream) {
+    int dev;
+    DeviceState *st;
+    int rc = device_state(&dev, &st);
+    if (rc != FA_OK) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_CUDA;
+    int word = 0, zero = 0;
+    if (cudaMemcpy(&word, st->status_word, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+    if (word != 0 && cudaMemcpy(st->status_word, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+        return FA_ERR_CUDA;
+    if (word == 0) return FA_OK;
+    return -(word & 0xFFFF);
+}
+
+namespace fa {
+namespace {
+// One warp waits on a barrier that nothing arrives on; the wait is bounded
+// and records FA_ERR_TIMEOUT when it runs out.
+__global__ void selftest_timeout_kernel(int *status, unsigned long long limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbarrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait(&bar, 0, status, 99, limit_ns);
+    __syncthreads();
+}
+}  // namespace
+
+cudaError_t launch_selftest_timeout(int *status, int limit_us, cudaStream_t s) {
+    selftest_timeout_kernel<<<1, 32, 0, s>>>(status, (unsigned long long)limit_us * 1000ull);
+    return cudaGetLastError();
+}
+}  // namespace fa
+
+extern "C" int fa_selftest_timeout(int limit_us, void *stream) {
+    if (limit_us < 1 || limit_us > 2000000) return FA_ERR_SHAPE;
+    int dev;
+    DeviceState *st;
+    int rc = device_state(&dev, &st);
+    if (rc != FA_OK) return rc;
+    cudaError_t e = launch_selftest_timeout(st->status_word, limit_us, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+extern "C" int fa_version(void) { return 100; }

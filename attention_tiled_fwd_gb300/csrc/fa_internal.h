@@ -1,0 +1,66 @@
+// fa_internal.h -- launch interfaces shared by the C-ABI layer (fa_api.cu) and
+// the kernel translation units.  Not part of the public ABI.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace fa {
+
+// Spec table for the tensor-core paths: query tile BM x key tile BN, K/V ring
+// depth, keyed by head dimension.  Picked so that S (double-buffered, BN
+// fp32 columns each) plus the D-column O accumulator fit the 512 TMEM
+// columns and the staged tiles fill (but do not exceed) shared memory.
+struct FwdSpec {
+    int D, BM, BN, nslot;
+};
+constexpr FwdSpec kFwdSpecs[] = {
+    {64, 128, 128, 8},   // Q 16 KB + 8 x 16 KB ring; TMEM 2x128 + 64
+    {128, 128, 128, 4},  // Q 32 KB + 4 x 32 KB ring; TMEM 2x128 + 128
+    {256, 128, 64, 4},   // Q 64 KB + 4 x 32 KB ring; TMEM 2x64 + 256 (D-blocked O)
+};
+
+struct FwdArgs {
+    const void *q, *k, *v;
+    void *o;
+    float *lse;
+    int B, H, N, D;
+    float scale;       // softmax scale
+    float scale_log2;  // scale * log2(e): scores go straight to the base-2 domain
+    int causal;
+    int *status;       // device status word (bounded-wait failures)
+};
+
+struct BwdArgs {
+    const void *q, *k, *v, *o, *dO;
+    const float *lse;
+    float *delta;        // written by the dQ kernel, read by the dK/dV kernel
+    void *dq, *dk, *dv;  // grad_dtype
+    int B, H, N, D;
+    float scale, scale_log2;
+    int causal;
+    int grad_bf16;  // 1: gradients stored as bf16, 0: fp32
+    int *status;
+};
+
+// Tensor maps for one [B*H, N, D] bf16 tensor, box = {64, rows, 1}, 128-byte swizzle.
+struct TmaPair {
+    CUtensorMap map;
+};
+
+cudaError_t launch_fwd_f32(const FwdArgs &a, cudaStream_t s);
+cudaError_t launch_fwd_bf16(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
+                            const CUtensorMap &tv, cudaStream_t s);
+cudaError_t launch_bwd_dq(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
+                          const CUtensorMap &tv, const CUtensorMap &tdo, cudaStream_t s);
+cudaError_t launch_bwd_dkdv(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
+                            const CUtensorMap &tv, const CUtensorMap &tdo, cudaStream_t s);
+cudaError_t launch_selftest_timeout(int *status, int limit_us, cudaStream_t s);
+
+inline int fwd_block_n(int D) {
+    for (const auto &sp : kFwdSpecs)
+        if (sp.D == D) return sp.BN;
+    return 0;
+}
+
+}  // namespace fa

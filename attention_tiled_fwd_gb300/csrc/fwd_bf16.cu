@@ -1,0 +1,340 @@
+// fwd_bf16.cu -- bf16 attention forward on the 5th-generation tensor cores
+// (tcgen05, accumulators in TMEM), K/V tiles streamed by TMA through an
+// mbarrier ring in shared memory.
+//
+// Algorithm ("Learning Metal with FlashAttention", section "FlashAttention";
+// metalworking "Flash Attention", kernel anatomy items 1-5; metal-flash-
+// attention forward pseudocode):
+//   Q tile loaded once and kept; for each K/V tile: S = Q K^T, scaled into
+//   the base-2 domain and masked in place, running max m / sum l, P = 2^(S-m),
+//   O <- alpha O + P V; after the last tile O /= l and L = m + ln(l) is
+//   written.  Causal tiles above the diagonal are never loaded or computed.
+//
+// GB300 mapping (one CTA = one 128-row query tile of one (batch, head)):
+//   warp 0      TMA producer: Q once, then K_j, V_j into an NSLOT-deep ring
+//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer:
+//                 S_j = Q K_j^T  (SS: both operands in shared memory) into one
+//                 of two S buffers in TMEM, then O += P_j V_j (TS: P_j, bf16, in
+//                 one of two P buffers in TMEM)
+//   warps 2-5   softmax: thread t owns query row t (TMEM lane t), so the row
+//               max / sum are thread-local; P is written back to TMEM as bf16.
+//               The O correction is lazy: O is rescaled only when the running
+//               max grows by more than 2^8 (the "branch-guarded correction"
+//               of the metalworking page), otherwise the stale max is kept;
+//               the final O / l is the same.
+//   TMEM: S0 [0, BN), S1 [BN, 2BN), O [2BN, 2BN + D), P0, P1 (BN/2 each)
+//   after O.  For D = 256 the O accumulator spans 256 columns and the PV
+//   product is one N = 256 MMA per 16-key step (D-blocking lives in the
+//   64-column panels of V and Q).
+//   Ordering: tcgen05.mma operations are only ordered among MMAs on the same
+//   accumulator, so no MMA ever writes TMEM columns an earlier MMA on another
+//   accumulator may still read.  P_j goes to P[j % 2]; the softmax writes it
+//   only after S_j completed, and the commit behind S_j tracks every earlier
+//   MMA, including PV_{j-2}, the last reader of P[j % 2].
+#include "fa_internal.h"
+#include "sm100_ptx.cuh"
+#include <cmath>
+
+namespace fa {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kThreads = 192;
+
+// Wait-site ids recorded in the status word on a time-out.
+enum : int { kSiteQ = 1, kSiteSlotEmpty, kSiteSlotFull, kSiteSFull, kSitePFull, kSitePV, kSiteFinal, kSiteDrain };
+
+template <int D, int BN, int NSLOT>
+struct FwdSmem {
+    static constexpr int kPanels = D / 64;
+    static constexpr int kQBytes = kBM * D * 2;
+    static constexpr int kSlotBytes = BN * D * 2;
+    static constexpr int kQOff = 0;
+    static constexpr int kSlotOff = kQBytes;
+    static constexpr int kBarOff = kSlotOff + NSLOT * kSlotBytes;
+    // barriers: q_full, slot_full[NSLOT], slot_empty[NSLOT], s_full[2], p_full[2], pv_done, final
+    static constexpr int kNumBars = 1 + 2 * NSLOT + 2 + 2 + 1 + 1;
+    static constexpr int kTmemHolderOff = kBarOff + kNumBars * 8;
+    static constexpr int kBytes = kTmemHolderOff + 16;
+    static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment of the base
+};
+
+template <int D, int BN, int NSLOT>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                    const __grid_constant__ CUtensorMap tmap_v, FwdArgs a) {
+    using L = FwdSmem<D, BN, NSLOT>;
+    constexpr int kPanels = L::kPanels;
+    constexpr uint32_t kTmemCols = 512;
+    constexpr uint32_t kColS0 = 0, kColS1 = BN, kColO = 2 * BN, kColP0 = 2 * BN + D, kColP1 = kColP0 + BN / 2;
+    static_assert(kColP1 + BN / 2 <= 512, "TMEM budget");
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *q_s = smem + L::kQOff;
+    uint8_t *slots = smem + L::kSlotOff;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
+    uint64_t *q_full = bars;
+    uint64_t *slot_full = bars + 1;
+    uint64_t *slot_empty = slot_full + NSLOT;
+    uint64_t *s_full = slot_empty + NSLOT;
+    uint64_t *p_full = s_full + 2;
+    uint64_t *pv_done = p_full + 2;
+    uint64_t *final_bar = pv_done + 1;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kTmemHolderOff);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q_tile = gridDim.x - 1 - blockIdx.x;  // heaviest causal tiles first
+    const int bh = blockIdx.z * a.H + blockIdx.y;
+    const int N = a.N;
+    const int kv_end = a.causal ? min(N, (q_tile + 1) * kBM) : N;
+    const int n_kv = (kv_end + BN - 1) / BN;  // >= 1 because q_tile * kBM < N
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < NSLOT; ++s) {
+            mbar_init(&slot_full[s], 1);
+            mbar_init(&slot_empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&s_full[b], 1);
+            mbar_init(&p_full[b], 128);
+        }
+        mbar_init(pv_done, 1);
+        mbar_init(final_bar, 1);
+        fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmap_q);
+            tma_prefetch_desc(&tmap_k);
+            tma_prefetch_desc(&tmap_v);
+            mbar_arrive_expect_tx(q_full, L::kQBytes);
+#pragma unroll
+            for (int p = 0; p < kPanels; ++p)
+                tma_load_3d(q_s + p * (kBM * 128), &tmap_q, q_full, p * 64, q_tile * kBM, bh);
+            int last_round[NSLOT];
+#pragma unroll
+            for (int s = 0; s < NSLOT; ++s) last_round[s] = -1;
+            for (int idx = 0; idx < 2 * n_kv; ++idx) {
+                const int slot = idx % NSLOT, round = idx / NSLOT;
+                if (!mbar_wait(&slot_empty[slot], (round & 1) ^ 1, a.status, kSiteSlotEmpty)) break;
+                uint8_t *dst = slots + slot * L::kSlotBytes;
+                const CUtensorMap *map = (idx & 1) ? &tmap_v : &tmap_k;
+                mbar_arrive_expect_tx(&slot_full[slot], L::kSlotBytes);
+#pragma unroll
+                for (int p = 0; p < kPanels; ++p)
+                    tma_load_3d(dst + p * (BN * 128), map, &slot_full[slot], p * 64, (idx >> 1) * BN, bh);
+#pragma unroll
+                for (int s = 0; s < NSLOT; ++s)
+                    if (s == slot) last_round[s] = round;
+            }
+            // Drain: never leave the CTA with a TMA write still in flight.
+#pragma unroll
+            for (int s = 0; s < NSLOT; ++s)
+                if (last_round[s] >= 0) mbar_wait(&slot_full[s], last_round[s] & 1, a.status, kSiteDrain);
+            mbar_wait(q_full, 0, a.status, kSiteDrain);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, BN, false, false);
+            constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, false, true);
+            const uint32_t q_addr = smem_u32(q_s);
+            const uint32_t slot_addr = smem_u32(slots);
+            bool ok = mbar_wait(q_full, 0, a.status, kSiteQ);
+            tc_fence_after();
+            auto issue_s = [&](int j) -> bool {
+                const int idx = 2 * j, slot = idx % NSLOT, round = idx / NSLOT;
+                if (!mbar_wait(&slot_full[slot], round & 1, a.status, kSiteSlotFull)) return false;
+                tc_fence_after();
+                const uint32_t kbase = slot_addr + slot * L::kSlotBytes;
+                const uint32_t d_s = tmem + ((j & 1) ? kColS1 : kColS0);
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks & 3) * 32;  // 16 bf16 = 32 B step inside the 128-B row
+                    const uint64_t ad = sdesc_sw128(q_addr + (ks >> 2) * (kBM * 128) + off, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(kbase + (ks >> 2) * (BN * 128) + off, 16, 1024);
+                    mma_ss(d_s, ad, bd, idesc_s, ks > 0);
+                }
+                mma_commit(&s_full[j & 1]);
+                mma_commit(&slot_empty[slot]);
+                return true;
+            };
+            if (ok) ok = issue_s(0);
+            if (ok && n_kv > 1) ok = issue_s(1);
+            for (int j = 0; ok && j < n_kv; ++j) {
+                if (!(ok = mbar_wait(&p_full[j & 1], (j >> 1) & 1, a.status, kSitePFull))) break;
+                tc_fence_after();
+                const int idx = 2 * j + 1, slot = idx % NSLOT, round = idx / NSLOT;
+                if (!(ok = mbar_wait(&slot_full[slot], round & 1, a.status, kSiteSlotFull))) break;
+                tc_fence_after();
+                const uint32_t vbase = slot_addr + slot * L::kSlotBytes;
+                const uint32_t p_t = tmem + ((j & 1) ? kColP1 : kColP0);
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    const uint64_t bd = sdesc_sw128(vbase + kk * 2048, BN * 128, 1024);
+                    mma_ts(tmem + kColO, p_t + kk * 8, bd, idesc_o, (j > 0 || kk > 0));
+                }
+                mma_commit(&slot_empty[slot]);
+                mma_commit(pv_done);
+                if (j + 2 < n_kv) ok = issue_s(j + 2);
+            }
+            // Every MMA issued above has completed before TMEM is released.
+            mma_commit(final_bar);
+            mbar_wait(final_bar, 0, a.status, kSiteFinal);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax / correction / epilogue
+        const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
+        const int r = quarter * 32 + lane;
+        const int row = q_tile * kBM + r;
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const float c = a.scale_log2;
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_kv; ++j) {
+            const uint32_t s_col = (j & 1) ? kColS1 : kColS0;
+            const uint32_t p_col = (j & 1) ? kColP1 : kColP0;
+            ok = mbar_wait(&s_full[j & 1], (j >> 1) & 1, a.status, kSiteSFull);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            tc_fence_after();
+            float s[BN];
+            {
+                uint32_t raw[32];
+#pragma unroll
+                for (int ch = 0; ch < BN / 32; ++ch) {
+                    tmem_ld32(tmem + lane_base + s_col + ch * 32, raw);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) s[ch * 32 + i] = __uint_as_float(raw[i]) * c;
+                }
+            }
+            const int key0 = j * BN;
+            const bool need_mask = (key0 + BN > N) || (a.causal && key0 + BN - 1 > q_tile * kBM);
+            if (need_mask) {
+                const int lim = a.causal ? min(N - 1, row) : N - 1;  // last visible key
+#pragma unroll
+                for (int i = 0; i < BN; ++i)
+                    if (key0 + i > lim) s[i] = -INFINITY;
+            }
+            float mt = s[0];
+#pragma unroll
+            for (int i = 1; i < BN; ++i) mt = fmaxf(mt, s[i]);
+            const float m_new = fmaxf(m, mt);
+            // Lazy correction: keep the stale max unless the row max grew by > 8 (factor 256).
+            const bool need = m_new > m + 8.f;
+            const float m_use = need ? m_new : m;
+            const float m_base = (m_use == -INFINITY) ? 0.f : m_use;
+            const float alpha = need ? ex2_approx(m - m_base) : 1.f;
+            float rs = 0.f;
+            // P = 2^(S - m) as bf16 pairs into this tile's P buffer.
+#pragma unroll
+            for (int ch = 0; ch < BN / 64; ++ch) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float p0 = ex2_approx(s[ch * 64 + 2 * i] - m_base);
+                    const float p1 = ex2_approx(s[ch * 64 + 2 * i + 1] - m_base);
+                    rs += p0 + p1;
+                    pk[i] = pack_bf16x2(p0, p1);
+                }
+                tmem_st32(tmem + lane_base + p_col + ch * 32, pk);
+            }
+            l = l * alpha + rs;
+            m = m_use;
+            if (j > 0 && __any_sync(0xffffffffu, need)) {
+                // O must hold P_{j-1} V_{j-1} before it is rescaled.
+                ok = mbar_wait(pv_done, (j - 1) & 1, a.status, kSitePV);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t ov[32];
+#pragma unroll
+                for (int ch = 0; ch < D / 32; ++ch) {
+                    tmem_ld32(tmem + lane_base + kColO + ch * 32, ov);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                    tmem_st32(tmem + lane_base + kColO + ch * 32, ov);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&p_full[j & 1]);
+        }
+        if (ok) {
+            ok = mbar_wait(pv_done, (n_kv - 1) & 1, a.status, kSitePV);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        if (ok) {
+            tc_fence_after();
+            const float inv_l = 1.f / l;
+            __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.o) + ((size_t)bh * N + row) * D;
+            uint32_t ov[32];
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch) {
+                tmem_ld32(tmem + lane_base + kColO + ch * 32, ov);
+                tmem_wait_ld();
+                if (row < N) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + ch * 32);
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(ov[v4 * 8 + 0]) * inv_l, __uint_as_float(ov[v4 * 8 + 1]) * inv_l);
+                        w.y = pack_bf16x2(__uint_as_float(ov[v4 * 8 + 2]) * inv_l, __uint_as_float(ov[v4 * 8 + 3]) * inv_l);
+                        w.z = pack_bf16x2(__uint_as_float(ov[v4 * 8 + 4]) * inv_l, __uint_as_float(ov[v4 * 8 + 5]) * inv_l);
+                        w.w = pack_bf16x2(__uint_as_float(ov[v4 * 8 + 6]) * inv_l, __uint_as_float(ov[v4 * 8 + 7]) * inv_l);
+                        dst[v4] = w;
+                    }
+                }
+            }
+            if (row < N) a.lse[(size_t)bh * N + row] = (m + __log2f(l)) * 0.69314718055994531f;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int D, int BN, int NSLOT>
+cudaError_t launch_spec(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                        cudaStream_t s) {
+    using L = FwdSmem<D, BN, NSLOT>;
+    static_assert(L::kAlloc <= 232448, "shared memory budget");
+    auto kern = fwd_bf16_kernel<D, BN, NSLOT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    if (e != cudaSuccess) return e;
+    dim3 grid((a.N + kBM - 1) / kBM, a.H, a.B);
+    kern<<<grid, kThreads, L::kAlloc, s>>>(tq, tk, tv, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_bf16(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                            cudaStream_t s) {
+    switch (a.D) {
+        case 64: return launch_spec<64, 128, 8>(a, tq, tk, tv, s);
+        case 128: return launch_spec<128, 128, 4>(a, tq, tk, tv, s);
+        case 256: return launch_spec<256, 64, 4>(a, tq, tk, tv, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace fa

@@ -1,0 +1,445 @@
+#!/usr/bin/env python
+"""Throughput benchmark of the tiled-attention hot path on GB300.
+
+One step = the whole path once over one batch of synthetic input:
+fa_forward (O, LSE) -> fa_backward_dq (delta, dQ) -> fa_backward_dkdv (dK, dV),
+bf16 inputs and gradients, fp32 accumulation.  Default workload: B=2 H=16
+N=4096 D=128 causal, the forward + split-backward case at D=128, N>=4096.
+
+Metric: attention TFLOP/s with the FLOPs counted algorithmically -- forward
+4 B H N^2 D, backward as its 7 GEMMs 14 B H N^2 D, both halved for causal.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-e2e] [--no-cpu-baseline]
+
+Timing: CUDA events on the launching stream around each kernel of each step;
+L2 is flushed (a 512 MB write) before every timed step, outside the events;
+a barrier + synchronize brackets the K timed steps; the job time is the max
+over ranks.  Multi-GPU (torchrun): every rank runs its own batch of the same
+shape (weak scaling, no collective on the data path).
+``--impl reference`` times the float64 CPU oracle on a bounded sample of the
+same workload on the host cores (the reference arm of this path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "bwd_bf16_b2h16n4096d128_causal"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------- host-side helpers (CPU-testable)
+def step_flops(B, H, N, D, causal, passes=("fwd", "bwd")) -> float:
+    per = (4.0 if "fwd" in passes else 0.0) + (14.0 if "bwd" in passes else 0.0)
+    f = per * B * H * float(N) * N * D
+    return f / 2 if causal else f
+
+
+def kernel_flops(B, H, N, D, causal):
+    c = 0.5 if causal else 1.0
+    u = B * H * float(N) * N * D * c
+    return {"fwd": 4 * u, "bwd_dq": 6 * u, "bwd_dkdv": 8 * u}
+
+
+def aggregate(local_seconds: float, local_flops: float, world: int, reduce_max=None, reduce_sum=None):
+    """Whole-job throughput: all ranks' FLOPs over the slowest rank's time."""
+    t = reduce_max(local_seconds) if reduce_max else local_seconds
+    f = reduce_sum(local_flops) if reduce_sum else local_flops * world
+    return f / t, t
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash(paths) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "fwd": ["attention_tiled_fwd_gb300/csrc/fwd_bf16.cu", "attention_tiled_fwd_gb300/csrc/sm100_ptx.cuh"],
+    "bwd_dq": ["attention_tiled_fwd_gb300/csrc/bwd_dq.cu", "attention_tiled_fwd_gb300/csrc/sm100_ptx.cuh"],
+    "bwd_dkdv": ["attention_tiled_fwd_gb300/csrc/bwd_dkdv.cu", "attention_tiled_fwd_gb300/csrc/sm100_ptx.cuh"],
+}
+
+
+def traffic_for(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current source."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload, {}).get(kernel)
+    if not e:
+        return None
+    cur = source_hash([os.path.join(ROOT, s) for s in KERNEL_SOURCES[kernel]])
+    return e["bytes_per_launch"] if e.get("source_hash") == cur else None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t_start = self.t_stop = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_stop(self):
+        self.t_stop = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for t, line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((t, parts))
+        inside = [r for r in rows if self.t_start is not None and self.t_start <= r[0] <= (self.t_stop or 1e30)]
+        used = inside if inside else rows[-2:]
+        mhz = [float(p[1]) for _, p in used if p[1].replace(".", "").isdigit()]
+        mx = [float(p[2]) for _, p in used if p[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, p in used for i in range(4) if p[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside),
+                "power_w_max": max((float(p[3]) for _, p in used if p[3].replace(".", "").isdigit()),
+                                   default=None)}
+
+
+# ----------------------------------------------------------------------------- CPU baseline (the oracle)
+def rows_flops(N, D, causal, i0, i1) -> float:
+    """Algorithmic FLOPs of query rows [i0, i1) of one head: (4 + 14) x visible keys x D per row."""
+    if causal:
+        nvis = (i1 * (i1 + 1) - i0 * (i0 + 1)) / 2.0
+    else:
+        nvis = float(i1 - i0) * N
+    return 18.0 * nvis * D
+
+
+class OracleSample:
+    """The float64 oracle's forward + backward over the last r query rows of `heads` heads of the
+    workload (one head per host thread), r sized so one run takes about target_s seconds."""
+
+    def __init__(self, w, threads: int):
+        import oracle
+        from synthetic_inputs import make_qkv
+        oracle.build()
+        self.oracle = oracle
+        self.w = w
+        self.threads = threads
+        self.heads = [(b, h) for b in range(w.B) for h in range(w.H)][:max(1, threads)]
+        self.inp = make_qkv(w.B, w.H, w.N, w.D, w.seed, w.dtype, w.std, with_dO=True)
+        self.rows = min(16, w.N)
+        self.run()  # calibration on a few rows
+
+    def size_for(self, target_s: float):
+        w = self.w
+        f_small, t_small = self.last
+        per_flop = t_small / max(f_small, 1.0)
+        # rows from the end of the head (the heaviest ones when causal): grow until the estimate fits
+        lo, hi = 1, w.N
+        while lo < hi:
+            mid = (lo + hi + 1) // 2
+            est = per_flop * rows_flops(w.N, w.D, w.causal[0], w.N - mid, w.N) * len(self.heads)
+            if est <= target_s:
+                lo = mid
+            else:
+                hi = mid - 1
+        self.rows = max(1, lo)
+
+    def run(self):
+        w = self.w
+        i0, i1 = w.N - self.rows, w.N
+        t0 = time.perf_counter()
+        self.oracle.backward_row_range(self.inp["q"], self.inp["k"], self.inp["v"], self.inp["dO"], w.scale,
+                                       w.causal[0], self.heads, i0, i1, threads=self.threads)
+        dt = time.perf_counter() - t0
+        f = rows_flops(w.N, w.D, w.causal[0], i0, i1) * len(self.heads)
+        self.last = (f, dt)
+        return f, dt
+
+    def describe(self, dt=None):
+        w = self.w
+        extra = f", {dt:.1f} s" if dt is not None else ""
+        return (f"query rows {w.N - self.rows}..{w.N - 1} of {len(self.heads)} of the {w.B * w.H} heads "
+                f"(N={w.N}, D={w.D}, causal={w.causal[0]}): float64 forward + backward terms of those rows, "
+                f"one head per host thread{extra}")
+
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return
+    cores = os.cpu_count() or 1
+    smp = OracleSample(w, cores)
+    per_step = max(0.5, min(8.0, 150.0 / (args.steps + args.warmup)))
+    smp.size_for(per_step)
+    times, flops = [], []
+    for it in range(args.warmup + args.steps):
+        f, dt = smp.run()
+        if it >= args.warmup:
+            times.append(dt)
+            flops.append(f)
+    total = sum(times)
+    value = sum(flops) / total / 1e12
+    line = {"impl": "reference", "metric": "attention fwd+bwd TFLOP/s (bf16; FLOPs 4 B H N^2 D fwd + 14 B H N^2 D "
+                                           "bwd (7 GEMMs), halved causal) and fraction of GB300 dense bf16 peak",
+            "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / len(times), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1))",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "causal": w.causal[0]},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": "each step: " + smp.describe()},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--grad-dtype", choices=("bf16", "f32"), default="bf16")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from synthetic_inputs import WORKLOADS, make_qkv
+    w = WORKLOADS[args.workload]
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+
+    import torch
+    import torch.distributed as dist
+    import attention_tiled_fwd_gb300 as fa
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def reduce_max(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def reduce_sum(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+        return float(t.item())
+
+    B, H, N, D = w.B, w.H, w.N, w.D
+    causal = w.causal[0]
+    passes = w.passes
+    scale = w.scale
+    gdt = torch.bfloat16 if args.grad_dtype == "bf16" else torch.float32
+    host = make_qkv(B, H, N, D, w.seed + 1000 * rank, w.dtype, w.std, with_dO="bwd" in passes)
+    q, k, v = (host[n].to(dev) for n in ("q", "k", "v"))
+    dO = host["dO"].to(dev) if "bwd" in passes else None
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    if "bwd" in passes:
+        dq = torch.empty((B, H, N, D), dtype=gdt, device=dev)
+        dk = torch.empty_like(dq)
+        dv = torch.empty_like(dq)
+        delta = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    kernels = ["fwd"] + (["bwd_dq", "bwd_dkdv"] if "bwd" in passes else [])
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        fa.fa_forward(q, k, v, scale=scale, causal=causal, o=o, lse=lse, stream=stream)
+        if "bwd" in passes:
+            if evs:
+                evs[1].record(stream)
+            fa.fa_backward_dq(q, k, v, o, dO, lse, scale=scale, causal=causal, dq=dq, delta=delta, stream=stream)
+            if evs:
+                evs[2].record(stream)
+            fa.fa_backward_dkdv(q, k, v, dO, lse, delta, scale=scale, causal=causal, dk=dk, dv=dv, stream=stream)
+        if evs:
+            evs[-1].record(stream)
+
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)  # > 129 MB L2
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    if fa.fa_device_status() != 0:
+        raise RuntimeError("device status reports a failure during warm-up")
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    nev = len(kernels) + 1
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    barrier()
+    sampler.mark_start()
+    for s in range(args.steps):
+        flush.fill_(float(s))
+        step(events[s])
+    barrier()
+    sampler.mark_stop()
+    clocks = sampler.stop()
+    if fa.fa_device_status() != 0:
+        raise RuntimeError("device status reports a failure in the timed region")
+
+    per_kernel = {kname: [] for kname in kernels}
+    step_ms = []
+    for evs in events:
+        for i, kname in enumerate(kernels):
+            per_kernel[kname].append(evs[i].elapsed_time(evs[i + 1]))
+        step_ms.append(evs[0].elapsed_time(evs[-1]))
+    local_s = sum(step_ms) / 1e3
+    flops = step_flops(B, H, N, D, causal, passes)
+    value, t_max = aggregate(local_s, flops * args.steps, world, reduce_max, reduce_sum)
+    kf = kernel_flops(B, H, N, D, causal)
+    mean_ms = {kname: statistics.mean(v_) for kname, v_ in per_kernel.items()}
+    kernel_tflops = {kname: kf[kname] / (mean_ms[kname] * 1e-3) / 1e12 for kname in kernels}
+    dom = max(kernels, key=lambda kn: mean_ms[kn])
+    peaks, peak_kind = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": kernel_tflops[dom], "peak": peak,
+                "unit": "TFLOP/s", "frac": kernel_tflops[dom] / peak, "traffic": traffic_for(dom, w.name),
+                "peak_source": f"{peak_kind} bf16_tflops (burst, cuBLAS bf16 GEMM)",
+                "peak_sustained": float(peaks.get("bf16_tflops_sustained", 0)) or None}
+
+    # ---- end to end through the public API: pinned host inputs in, results back out
+    e2e = None
+    if not args.no_e2e:
+        pin = {n: t.pin_memory() for n, t in host.items()}
+        outs = {"o": torch.empty_like(o, device="cpu").pin_memory()}
+        if "bwd" in passes:
+            for n in ("dq", "dk", "dv"):
+                outs[n] = torch.empty((B, H, N, D), dtype=gdt).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in pin.values())
+        d2h = sum(t.numel() * t.element_size() for t in outs.values())
+        n_e2e = max(3, min(args.steps, 50))
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            q.copy_(pin["q"], non_blocking=True)
+            k.copy_(pin["k"], non_blocking=True)
+            v.copy_(pin["v"], non_blocking=True)
+            if dO is not None:
+                dO.copy_(pin["dO"], non_blocking=True)
+            step()
+            outs["o"].copy_(o, non_blocking=True)
+            if "bwd" in passes:
+                outs["dq"].copy_(dq, non_blocking=True)
+                outs["dk"].copy_(dk, non_blocking=True)
+                outs["dv"].copy_(dv, non_blocking=True)
+        e1.record(stream)
+        barrier()
+        e2e_s = e0.elapsed_time(e1) / 1e3
+        e2e_val, _ = aggregate(e2e_s, flops * n_e2e, world, reduce_max, reduce_sum)
+        e2e = {"value": e2e_val / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": n_e2e}
+
+    cpu_baseline = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cores = os.cpu_count() or 1
+        smp = OracleSample(w, cores)
+        smp.size_for(15.0)
+        f, dt = smp.run()
+        cpu_baseline = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                        "sample": smp.describe(dt)}
+
+    if rank == 0:
+        line = {
+            "metric": "attention fwd+bwd TFLOP/s (bf16; FLOPs 4 B H N^2 D fwd + 14 B H N^2 D bwd (7 GEMMs), "
+                      "halved causal) and fraction of GB300 dense bf16 peak",
+            "value": value / 1e12, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * t_max / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1), per-rank seed)",
+            "config": {"workload": w.name, "B": B, "H": H, "N": N, "D": D, "causal": causal, "passes": list(passes),
+                       "grad_dtype": args.grad_dtype, "global_batch": B * world, "seq_len": N,
+                       "parallelism": f"replicas x{world} (independent batches)",
+                       "l2": "flushed before every timed step (512 MB write), outside the timed events"},
+            "kernels": {kn: {"ms": mean_ms[kn], "tflops": kernel_tflops[kn],
+                             "frac_of_peak": kernel_tflops[kn] / peak} for kn in kernels},
+            "roofline": roofline,
+            "cpu_baseline": cpu_baseline,
+            "e2e": e2e,
+            "gpu_launches": len(kernels) * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

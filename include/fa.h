@@ -1,0 +1,137 @@
+/*
+ * fa.h -- C ABI of libfa: exact scaled-dot-product attention on one GB300
+ * (sm_103a), computed tile by tile (FlashAttention style), with the
+ * atomic-free split backward.
+ *
+ * Operation (all entry points):
+ *   Per (batch b, head h) slice, Q, K, V, O, dO are N x D matrices and
+ *     S = scale * Q K^T,  P = softmax_row(S)  (causal: key j visible to query
+ *     row i iff j <= i),  O = P V,  LSE_i = ln sum_j exp(S_ij).
+ *   Definition and streaming form: "Learning Metal with FlashAttention",
+ *   section "FlashAttention" (per-row softmax over all keys; running max,
+ *   running sum and unnormalised output updated per K/V tile; O divided by
+ *   the sum after the last tile).  Causal tiles skipped rather than masked,
+ *   base-2 exponent: "Flash Attention" (metalworking), kernel anatomy items
+ *   3-4.  LSE = m + ln(l) and the split backward (one dQ kernel, one dK/dV
+ *   kernel, 7 GEMMs, no atomics): "FlashAttention (Metal port)"
+ *   (metal-flash-attention), documentation section and the forward /
+ *   backward pseudocode of its performance section.
+ *
+ * Memory layout and ownership (all entry points):
+ *   - q, k, v, o, dO, dq, dk, dv: [B, H, N, D] contiguous, row-major, in
+ *     DEVICE memory allocated by the caller, 16-byte aligned.
+ *   - lse, delta: [B, H, N] contiguous float32 in device memory.
+ *   - The library never allocates, frees or retains caller memory; outputs
+ *     are fully overwritten (rows 0..N-1 of every head).
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
+ *     void*; NULL is the legacy default stream).  No entry point
+ *     synchronises the host except fa_device_status().
+ *
+ * Errors: every entry point returns FA_OK (0) or a negative fa_status.
+ * Arguments are validated before anything is launched; on a validation
+ * error nothing is enqueued and no output is touched.  A launch failure
+ * reported by the CUDA runtime is returned as FA_ERR_CUDA.  Kernels never
+ * trap: every wait inside a kernel is bounded, and a wait that runs out
+ * records FA_ERR_TIMEOUT in a device status word which fa_device_status()
+ * reads (outputs of that launch are then undefined).
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types of q/k/v/o/dO (dtype) and of dq/dk/dv (grad_dtype). */
+enum fa_dtype {
+    FA_F32 = 0,   /* IEEE float32                                      */
+    FA_BF16 = 1   /* bfloat16, round-to-nearest-even on every store    */
+};
+
+enum fa_status {
+    FA_OK = 0,
+    FA_ERR_NULL = -1,        /* a required pointer is NULL                              */
+    FA_ERR_SHAPE = -2,       /* B, H or N < 1, or B*H*N*D overflows the index range      */
+    FA_ERR_HEAD_DIM = -3,    /* D not supported for this dtype / pass (see below)        */
+    FA_ERR_DTYPE = -4,       /* unknown dtype / grad_dtype, or an unsupported pairing   */
+    FA_ERR_ALIGN = -5,       /* a pointer is not 16-byte aligned                         */
+    FA_ERR_SCALE = -6,       /* scale is not finite                                      */
+    FA_ERR_CUDA = -7,        /* the CUDA runtime reported an error (launch, attributes)  */
+    FA_ERR_TIMEOUT = -8,     /* a bounded in-kernel wait ran out (read by fa_device_status) */
+    FA_ERR_DEVICE_PTR = -9,  /* a pointer is not device-accessible memory                */
+    FA_ERR_DEVICE = -10      /* the current device is not sm_100-family (tcgen05)        */
+};
+
+/*
+ * fa_forward -- O = softmax(scale Q K^T) V and LSE (natural log-sum-exp of the
+ * scaled scores of each row).
+ *   dtype FA_BF16: D in {64, 128, 256}; bf16 inputs, fp32 accumulation
+ *                  (tcgen05 tensor cores), bf16 O, fp32 LSE.
+ *   dtype FA_F32 : D a multiple of 32 in [32, 256]; fp32 inputs and O,
+ *                  fp32 FFMA arithmetic throughout, fp32 LSE.
+ *   N >= 1 arbitrary (ragged tails are masked).  causal: 0 or non-zero.
+ */
+FA_API int fa_forward(const void *q, const void *k, const void *v, void *o, float *lse,
+               int B, int H, int N, int D, float scale, int causal, int dtype,
+               void *stream);
+
+/*
+ * fa_backward_dq -- first half of the split backward ("backward query"):
+ *   delta_i = sum_d dO_id O_id            (written: delta [B,H,N] fp32)
+ *   P = exp(S - LSE), dP = dO V^T, dS = P * (dP - delta) * scale,
+ *   dQ = dS K                              (written: dq, grad_dtype)
+ * o and lse are the outputs of fa_forward on the same q, k, v, scale, causal.
+ * Supported: dtype FA_BF16 with D in {64, 128}; grad_dtype FA_F32 or FA_BF16.
+ */
+FA_API int fa_backward_dq(const void *q, const void *k, const void *v, const void *o,
+                   const void *dO, const float *lse, float *delta, void *dq,
+                   int B, int H, int N, int D, float scale, int causal, int dtype,
+                   int grad_dtype, void *stream);
+
+/*
+ * fa_backward_dkdv -- second half ("backward key-value"), one CTA per K/V
+ * tile iterating over query tiles:
+ *   P^T = exp(S^T - LSE), dV = P^T dO, dP^T = V dO^T,
+ *   dS^T = P^T * (dP^T - delta) * scale, dK = dS^T Q
+ * lse from fa_forward, delta from fa_backward_dq (enqueue this call after it
+ * on the same stream, or order the two streams yourself).
+ * Supported: dtype FA_BF16 with D in {64, 128}; grad_dtype FA_F32 or FA_BF16.
+ */
+FA_API int fa_backward_dkdv(const void *q, const void *k, const void *v, const void *dO,
+                     const float *lse, const float *delta, void *dk, void *dv,
+                     int B, int H, int N, int D, float scale, int causal, int dtype,
+                     int grad_dtype, void *stream);
+
+/* Static description of a status code (never NULL). */
+FA_API const char *fa_status_string(int status);
+
+/*
+ * fa_device_status -- synchronises `stream`, then returns and clears the
+ * device status word of the current device: FA_OK, or FA_ERR_TIMEOUT if a
+ * bounded in-kernel wait ran out since the last call.  Returns FA_ERR_CUDA
+ * if the synchronisation itself failed.
+ */
+FA_API int fa_device_status(void *stream);
+
+/*
+ * fa_selftest_timeout -- test hook for the failure path: launches one
+ * 32-thread block that waits on a shared-memory barrier nothing arrives on,
+ * with a wait bounded by limit_us microseconds (1..2000000); the kernel
+ * records FA_ERR_TIMEOUT and returns.  Returns FA_OK if launched.
+ */
+FA_API int fa_selftest_timeout(int limit_us, void *stream);
+
+/* Library version (major*10000 + minor*100 + patch). */
+FA_API int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -59,6 +59,10 @@ def _load():
             lib.fa_oracle_backward_head.argtypes = [_dp, _dp, _dp, _dp, ctypes.c_int64, ctypes.c_int64,
                                                     ctypes.c_double, ctypes.c_int, _dp, _dp, _dp,
                                                     _dp, _dp, _dp]
+            lib.fa_oracle_backward_head_rows.argtypes = [_dp, _dp, _dp, _dp, ctypes.c_int64, ctypes.c_int64,
+                                                         ctypes.c_double, ctypes.c_int, ctypes.c_int64,
+                                                         ctypes.c_int64, _dp, _dp, _dp, _dp, _dp, _dp]
+            lib.fa_oracle_backward_head_rows.restype = ctypes.c_int
             lib.fa_oracle_backward_dq_rows.argtypes = [_dp, _dp, _dp, _dp, ctypes.c_int64,
                                                        ctypes.c_int64, ctypes.c_double, ctypes.c_int,
                                                        ctypes.c_int64, _ip, _dp, _dp]
@@ -137,6 +141,35 @@ def backward(q, k, v, dO, scale: float, causal: bool, threads: Optional[int] = N
                                            _ptr(out["dk"][b, h]), _ptr(out["dv"][b, h])), "backward")
 
     _map_heads(one, [(b, h) for b in range(B) for h in range(H)], threads)
+    return out
+
+
+def backward_row_range(q, k, v, dO, scale: float, causal: bool, heads: Sequence[Tuple[int, int]],
+                       row_begin: int, row_end: int, threads: Optional[int] = None):
+    """Forward + backward terms of query rows [row_begin, row_end) for each listed (b, h) head.
+
+    Returns {(b, h): dict(o, lse, delta, dq, dk, dv)} where o/lse/delta/dq hold those rows
+    and dk/dv hold those rows' contributions (the full gradients when the range is 0..N).
+    """
+    D = q.shape[-1]
+    N = q.shape[-2]
+    lib = _load()
+    out = {}
+
+    def one(bh):
+        b, h = bh
+        qi, ki, vi, di = _f64(q[b, h]), _f64(k[b, h]), _f64(v[b, h]), _f64(dO[b, h])
+        r = {"o": np.zeros((N, D)), "lse": np.zeros((N,)), "delta": np.zeros((N,)),
+             "dq": np.zeros((N, D)), "dk": np.zeros((N, D)), "dv": np.zeros((N, D))}
+        _check(lib.fa_oracle_backward_head_rows(_ptr(qi), _ptr(ki), _ptr(vi), _ptr(di), N, D, float(scale),
+                                                int(bool(causal)), int(row_begin), int(row_end),
+                                                _ptr(r["o"]), _ptr(r["lse"]), _ptr(r["delta"]), _ptr(r["dq"]),
+                                                _ptr(r["dk"]), _ptr(r["dv"])), "backward_row_range")
+        for n in ("o", "lse", "delta", "dq"):
+            r[n] = r[n][row_begin:row_end]
+        out[bh] = r
+
+    _map_heads(one, list(heads), threads)
     return out
 
 

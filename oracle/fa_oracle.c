@@ -95,30 +95,35 @@ int fa_oracle_forward_rows(const double *q, const double *k, const double *v,
         int64_t nvis = visible_keys(i, N, causal);
         score_row(q + i * D, k, nvis, D, scale, p);
         lse[r] = softmax_row(p, nvis);
-        for (int64_t d = 0; d < D; ++d) {
-            double acc = 0.0;
-            for (int64_t j = 0; j < nvis; ++j)
-                acc += p[j] * v[j * D + d];
-            o[r * D + d] = acc;
-        }
+        /* O_i = sum_j P_ij v_j */
+        for (int64_t d = 0; d < D; ++d)
+            o[r * D + d] = 0.0;
+        for (int64_t j = 0; j < nvis; ++j)
+            for (int64_t d = 0; d < D; ++d)
+                o[r * D + d] += p[j] * v[j * D + d];
     }
     free(p);
     return 0;
 }
 
 /*
- * Full forward + backward of one head, the plain definition row by row.
+ * Forward + backward contributions of query rows [row_begin, row_end) of one
+ * head, the plain definition row by row.  For each such row i it writes
+ * o[i], lse[i], delta[i], dq[i] and ADDS row i's terms to dk and dv (the
+ * caller zeroes them; over all rows 0..N-1 they become the full gradients).
  *   o, lse        : [N, D], [N]      forward outputs (float64, exact up to rounding)
  *   delta         : [N]              D_i = sum_d dO_id * O_id (this oracle's own O)
  *   dq, dk, dv    : [N, D]           gradients of sum(O * dO)
- * Any output pointer may be NULL except dk/dv/dq, which are always written.
+ * o, lse and delta may be NULL.
  */
-int fa_oracle_backward_head(const double *q, const double *k, const double *v,
-                            const double *dO, int64_t N, int64_t D, double scale,
-                            int causal, double *o, double *lse, double *delta,
-                            double *dq, double *dk, double *dv)
+int fa_oracle_backward_head_rows(const double *q, const double *k, const double *v,
+                                 const double *dO, int64_t N, int64_t D, double scale,
+                                 int causal, int64_t row_begin, int64_t row_end,
+                                 double *o, double *lse, double *delta,
+                                 double *dq, double *dk, double *dv)
 {
-    if (N < 1 || D < 1 || !dq || !dk || !dv)
+    if (N < 1 || D < 1 || !dq || !dk || !dv || row_begin < 0 || row_end > N ||
+        row_begin > row_end)
         return -1;
     double *p = (double *)malloc((size_t)N * sizeof(double));
     double *orow = (double *)malloc((size_t)D * sizeof(double));
@@ -127,9 +132,7 @@ int fa_oracle_backward_head(const double *q, const double *k, const double *v,
         free(orow);
         return -1;
     }
-    memset(dk, 0, (size_t)(N * D) * sizeof(double));
-    memset(dv, 0, (size_t)(N * D) * sizeof(double));
-    for (int64_t i = 0; i < N; ++i) {
+    for (int64_t i = row_begin; i < row_end; ++i) {
         int64_t nvis = visible_keys(i, N, causal);
         const double *q_i = q + i * D;
         const double *do_i = dO + i * D;
@@ -137,12 +140,11 @@ int fa_oracle_backward_head(const double *q, const double *k, const double *v,
         score_row(q_i, k, nvis, D, scale, p);
         double lse_i = softmax_row(p, nvis);
         /* O_i = sum_j P_ij v_j */
-        for (int64_t d = 0; d < D; ++d) {
-            double acc = 0.0;
-            for (int64_t j = 0; j < nvis; ++j)
-                acc += p[j] * v[j * D + d];
-            orow[d] = acc;
-        }
+        for (int64_t d = 0; d < D; ++d)
+            orow[d] = 0.0;
+        for (int64_t j = 0; j < nvis; ++j)
+            for (int64_t d = 0; d < D; ++d)
+                orow[d] += p[j] * v[j * D + d];
         /* D_i = sum_d dO_id O_id */
         double delta_i = 0.0;
         for (int64_t d = 0; d < D; ++d)
@@ -171,6 +173,20 @@ int fa_oracle_backward_head(const double *q, const double *k, const double *v,
     free(p);
     free(orow);
     return 0;
+}
+
+/* Full forward + backward of one head: all rows of fa_oracle_backward_head_rows. */
+int fa_oracle_backward_head(const double *q, const double *k, const double *v,
+                            const double *dO, int64_t N, int64_t D, double scale,
+                            int causal, double *o, double *lse, double *delta,
+                            double *dq, double *dk, double *dv)
+{
+    if (N < 1 || D < 1 || !dq || !dk || !dv)
+        return -1;
+    memset(dk, 0, (size_t)(N * D) * sizeof(double));
+    memset(dv, 0, (size_t)(N * D) * sizeof(double));
+    return fa_oracle_backward_head_rows(q, k, v, dO, N, D, scale, causal, 0, N, o, lse, delta,
+                                        dq, dk, dv);
 }
 
 /*
@@ -203,12 +219,11 @@ int fa_oracle_backward_dq_rows(const double *q, const double *k, const double *v
         const double *do_i = dO + i * D;
         score_row(q + i * D, k, nvis, D, scale, p);
         softmax_row(p, nvis);
-        for (int64_t d = 0; d < D; ++d) {
-            double acc = 0.0;
-            for (int64_t j = 0; j < nvis; ++j)
-                acc += p[j] * v[j * D + d];
-            orow[d] = acc;
-        }
+        for (int64_t d = 0; d < D; ++d)
+            orow[d] = 0.0;
+        for (int64_t j = 0; j < nvis; ++j)
+            for (int64_t d = 0; d < D; ++d)
+                orow[d] += p[j] * v[j * D + d];
         double delta_i = 0.0;
         for (int64_t d = 0; d < D; ++d)
             delta_i += do_i[d] * orow[d];

@@ -1,0 +1,46 @@
+"""Shared helpers for the parity tests: device set-up, tolerance checks, oracle calls."""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+# Tolerances (stated in the attention path's target): fp32 O max-abs 1e-4;
+# bf16 O / dQ / dK / dV max-abs 2e-2; LSE 1e-3.  Outputs *stored* in bf16 add
+# one bf16 rounding of the reference value (2^-8 relative) on top of the flat
+# bound, since storing |x| in [8, 16) alone can move it by 2^-5.
+TOL_F32 = 1e-4
+TOL_BF16 = 2e-2
+TOL_LSE = 1e-3
+BF16_REL = 2.0 ** -8
+
+
+def cuda_or_skip():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import attention_tiled_fwd_gb300 as fa  # noqa: F401  (fails loudly if libfa.so is missing)
+    return torch.device("cuda:0")
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to("cpu").double().numpy()
+
+
+def assert_close(got, ref, atol: float, rel: float = 0.0, what: str = ""):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    assert np.isfinite(got).all(), f"{what}: non-finite values"
+    err = np.abs(got - ref)
+    bound = atol + rel * np.abs(ref)
+    worst = float((err - bound).max()) if err.size else -1.0
+    if worst > 0:
+        idx = np.unravel_index(np.argmax(err - bound), err.shape)
+        raise AssertionError(f"{what}: |err| {err[idx]:.3e} > bound {bound[idx]:.3e} at {idx} "
+                             f"(got {got[idx]:.6f}, ref {ref[idx]:.6f}); max |err| {err.max():.3e}")
+    return float(err.max()) if err.size else 0.0

@@ -255,6 +255,23 @@ def test_row_variants_agree_with_full(causal):
         np.testing.assert_allclose(dv[n], g["dv"][b, h, i], atol=1e-12)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_ranges_sum_to_full_backward(causal):
+    """The row-range form: rows [0, a) plus rows [a, N) give the full-head gradients."""
+    B, H, N, D = 1, 2, 23, 4
+    q, k, v, dO = (_rand((B, H, N, D), 90 + s) for s in range(4))
+    g = oracle.backward(q, k, v, dO, 0.7, causal)
+    heads = [(0, 0), (0, 1)]
+    lo = oracle.backward_row_range(q, k, v, dO, 0.7, causal, heads, 0, 9)
+    hi = oracle.backward_row_range(q, k, v, dO, 0.7, causal, heads, 9, N)
+    for b, h in heads:
+        np.testing.assert_allclose(lo[(b, h)]["dk"] + hi[(b, h)]["dk"], g["dk"][b, h], atol=1e-12)
+        np.testing.assert_allclose(lo[(b, h)]["dv"] + hi[(b, h)]["dv"], g["dv"][b, h], atol=1e-12)
+        np.testing.assert_allclose(np.concatenate([lo[(b, h)]["dq"], hi[(b, h)]["dq"]]), g["dq"][b, h],
+                                   atol=1e-12)
+        np.testing.assert_allclose(hi[(b, h)]["o"], g["o"][b, h, 9:], atol=1e-13)
+
+
 def test_rejects_bad_arguments():
     q = np.zeros((1, 1, 4, 2))
     with pytest.raises(RuntimeError):

@@ -1,0 +1,127 @@
+"""GPU forward vs the float64 oracle, element by element, through the C ABI.
+
+Small shapes (oracle in full) span several tiles and ragged tails; the
+full-size workloads are checked on seeded sampled rows, which the oracle
+computes one by one over the whole key range.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import TOL_BF16, TOL_F32, TOL_LSE, BF16_REL, assert_close, cuda_or_skip, to_np
+from synthetic_inputs import WORKLOADS, make_qkv, sample_rows, workload_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_fwd(inp, causal, dev, scale=None):
+    import attention_tiled_fwd_gb300 as fa
+    q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+    o, lse = fa.fa_forward(q, k, v, scale=scale, causal=causal)
+    assert fa.fa_device_status() == 0
+    return o, lse
+
+
+def test_fp32_forward_small_workload():
+    """fp32, B=1 H=1 N=256 D=64, non-causal: O within 1e-4, LSE within 1e-3 (the oracle in full)."""
+    dev = cuda_or_skip()
+    w = WORKLOADS["fwd_f32_b1h1n256d64"]
+    inp = workload_inputs(w)
+    for causal in (False, True):
+        o, lse = _run_fwd(inp, causal, dev, w.scale)
+        ro, rl = oracle.forward(inp["q"], inp["k"], inp["v"], w.scale, causal)
+        assert_close(to_np(o), ro, TOL_F32, what=f"fp32 O causal={causal}")
+        assert_close(to_np(lse), rl, 1e-5, what=f"fp32 LSE causal={causal}")
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1, 64), (1, 2, 45, 32), (2, 1, 300, 128), (1, 1, 129, 256),
+                                   (1, 1, 200, 96)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp32_forward_edge_shapes(shape, causal):
+    dev = cuda_or_skip()
+    B, H, N, D = shape
+    inp = make_qkv(B, H, N, D, seed=11 + N + D, dtype="f32")
+    scale = 1.0 / np.sqrt(D)
+    o, lse = _run_fwd(inp, causal, dev, scale)
+    ro, rl = oracle.forward(inp["q"], inp["k"], inp["v"], scale, causal)
+    assert_close(to_np(o), ro, TOL_F32, what="fp32 O")
+    assert_close(to_np(lse), rl, 1e-5, what="fp32 LSE")
+
+
+# Several query and key tiles, ragged tails (N not a multiple of 128 or 64), N < tile, N = 1.
+BF16_SHAPES = [(1, 1, 1, 64), (1, 2, 77, 64), (1, 1, 128, 128), (2, 2, 300, 64), (1, 2, 257, 128),
+               (1, 1, 383, 128), (1, 1, 129, 256), (1, 2, 320, 256), (2, 1, 640, 128)]
+
+
+@pytest.mark.parametrize("shape", BF16_SHAPES)
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_forward_small_shapes(shape, causal):
+    dev = cuda_or_skip()
+    B, H, N, D = shape
+    inp = make_qkv(B, H, N, D, seed=100 + N + D, dtype="bf16")
+    scale = 1.0 / np.sqrt(D)
+    o, lse = _run_fwd(inp, causal, dev, scale)
+    ro, rl = oracle.forward(inp["q"], inp["k"], inp["v"], scale, causal)
+    assert_close(to_np(o), ro, TOL_BF16, BF16_REL, what="bf16 O")
+    assert_close(to_np(lse), rl, TOL_LSE, what="bf16 LSE")
+
+
+def test_bf16_forward_scale_and_large_logits():
+    """A large scale drives scores far apart (the lazy-rescale path and max updates late in the row)."""
+    dev = cuda_or_skip()
+    inp = make_qkv(1, 2, 513, 128, seed=7, dtype="bf16", std=1.0)
+    for scale, causal in ((0.5, False), (0.5, True), (0.02, False)):
+        o, lse = _run_fwd(inp, causal, dev, scale)
+        ro, rl = oracle.forward(inp["q"], inp["k"], inp["v"], scale, causal)
+        assert_close(to_np(o), ro, TOL_BF16, BF16_REL, what=f"bf16 O scale={scale}")
+        assert_close(to_np(lse), rl, TOL_LSE, what=f"bf16 LSE scale={scale}")
+
+
+def test_bf16_forward_increasing_logits_force_rescale():
+    """Keys whose scores grow along the row make the running max rise on every tile."""
+    dev = cuda_or_skip()
+    B, H, N, D = 1, 1, 700, 64
+    g = torch.Generator().manual_seed(5)
+    q = torch.ones(B, H, N, D)
+    k = (torch.arange(N).float()[None, None, :, None] / N * 3.0).expand(B, H, N, D).contiguous()
+    k = k + 0.01 * torch.randn(B, H, N, D, generator=g)
+    v = torch.randn(B, H, N, D, generator=g)
+    inp = {n: t.to(torch.bfloat16).contiguous() for n, t in (("q", q), ("k", k), ("v", v))}
+    for causal in (False, True):
+        o, lse = _run_fwd(inp, causal, dev, 1.0)
+        ro, rl = oracle.forward(inp["q"], inp["k"], inp["v"], 1.0, causal)
+        assert_close(to_np(o), ro, TOL_BF16, BF16_REL, what="bf16 O rising max")
+        assert_close(to_np(lse), rl, TOL_LSE, what="bf16 LSE rising max")
+
+
+def test_bf16_forward_is_deterministic():
+    dev = cuda_or_skip()
+    inp = make_qkv(2, 2, 1000, 128, seed=3, dtype="bf16")
+    o1, l1 = _run_fwd(inp, True, dev)
+    o2, l2 = _run_fwd(inp, True, dev)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("name,causal", [("fwd_bf16_b4h16n2048d128", False), ("fwd_bf16_b4h16n2048d128", True),
+                                         ("fwd_bf16_b1h8n8192d256", False),
+                                         ("bwd_bf16_b2h16n4096d128_causal", True),
+                                         ("fwdbwd_bf16_b1h32n32768d64_causal", True)])
+def test_bf16_forward_full_size_sampled_rows(name, causal):
+    """Full-size workloads in the launch configuration the benchmark times; 256 seeded rows
+    (plus tile-edge rows) checked against float64 full-row references."""
+    dev = cuda_or_skip()
+    w = WORKLOADS[name]
+    inp = workload_inputs(w, with_dO=False)
+    o, lse = _run_fwd(inp, causal, dev, w.scale)
+    rows = sample_rows(w.B, w.H, w.N, 256, seed=w.seed)
+    ro, rl = oracle.forward_rows(inp["q"], inp["k"], inp["v"], w.scale, causal, rows)
+    idx = tuple(np.array(rows).T)
+    go = o[idx].double().cpu().numpy()
+    gl = lse[idx].double().cpu().numpy()
+    assert_close(go, ro, TOL_BF16, BF16_REL, what=f"{name} O")
+    assert_close(gl, rl, TOL_LSE, what=f"{name} LSE")
+    # properties at every row: finite, and each O row lies in the hull of V's rows (|O| <= max |V|)
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    vmax = inp["v"].abs().amax().item()
+    assert o.abs().amax().item() <= vmax * (1 + 2 ** -7)

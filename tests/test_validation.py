@@ -1,0 +1,113 @@
+"""Argument validation of the C ABI.  Shape, dtype, head-dimension, scale,
+NULL and alignment checks run before any CUDA call, so these need no GPU;
+the device-pointer and device-status checks run on the GPU."""
+import ctypes
+import math
+
+import pytest
+
+from attention_tiled_fwd_gb300 import _native as nat
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from attention_tiled_fwd_gb300 import build
+    build.build()
+    return nat.load()
+
+
+A = 4096  # a fake, 16-byte-aligned address: validation must reject the call before touching it
+
+
+def fwd(lib, q=A, k=A, v=A, o=A, lse=A, B=1, H=1, N=8, D=64, scale=0.125, causal=0, dtype=nat.FA_BF16):
+    return lib.fa_forward(q, k, v, o, lse, B, H, N, D, scale, causal, dtype, None)
+
+
+def test_forward_rejects_bad_shapes(lib):
+    assert fwd(lib, B=0) == nat.FA_ERR_SHAPE
+    assert fwd(lib, H=0) == nat.FA_ERR_SHAPE
+    assert fwd(lib, N=0) == nat.FA_ERR_SHAPE
+    assert fwd(lib, N=-5) == nat.FA_ERR_SHAPE
+    assert fwd(lib, B=70000) == nat.FA_ERR_SHAPE
+    assert fwd(lib, B=65535, H=65535, N=65535) == nat.FA_ERR_SHAPE
+
+
+def test_forward_rejects_head_dims(lib):
+    for D in (0, 16, 32, 96, 100, 192, 512):
+        assert fwd(lib, D=D) in (nat.FA_ERR_HEAD_DIM, nat.FA_ERR_SHAPE), D
+    for D in (48, 100, 288):
+        assert fwd(lib, D=D, dtype=nat.FA_F32) == nat.FA_ERR_HEAD_DIM, D
+
+
+def test_forward_rejects_dtype_scale_null_align(lib):
+    assert fwd(lib, dtype=7) == nat.FA_ERR_DTYPE
+    assert fwd(lib, scale=math.inf) == nat.FA_ERR_SCALE
+    assert fwd(lib, scale=math.nan) == nat.FA_ERR_SCALE
+    assert fwd(lib, q=None) == nat.FA_ERR_NULL
+    assert fwd(lib, lse=None) == nat.FA_ERR_NULL
+    assert fwd(lib, o=A + 2) == nat.FA_ERR_ALIGN
+    assert fwd(lib, k=A + 8) == nat.FA_ERR_ALIGN
+
+
+def test_backward_rejects(lib):
+    def dq(**kw):
+        a = dict(q=A, k=A, v=A, o=A, dO=A, lse=A, delta=A, dq=A, B=1, H=1, N=8, D=128, scale=0.1, causal=1,
+                 dtype=nat.FA_BF16, grad=nat.FA_F32)
+        a.update(kw)
+        return lib.fa_backward_dq(a["q"], a["k"], a["v"], a["o"], a["dO"], a["lse"], a["delta"], a["dq"], a["B"],
+                                  a["H"], a["N"], a["D"], a["scale"], a["causal"], a["dtype"], a["grad"], None)
+
+    def dkdv(**kw):
+        a = dict(q=A, k=A, v=A, dO=A, lse=A, delta=A, dk=A, dv=A, B=1, H=1, N=8, D=64, scale=0.1, causal=0,
+                 dtype=nat.FA_BF16, grad=nat.FA_BF16)
+        a.update(kw)
+        return lib.fa_backward_dkdv(a["q"], a["k"], a["v"], a["dO"], a["lse"], a["delta"], a["dk"], a["dv"],
+                                    a["B"], a["H"], a["N"], a["D"], a["scale"], a["causal"], a["dtype"],
+                                    a["grad"], None)
+
+    assert dq(D=256) == nat.FA_ERR_HEAD_DIM
+    assert dq(D=32) == nat.FA_ERR_HEAD_DIM
+    assert dq(grad=5) == nat.FA_ERR_DTYPE
+    assert dq(dtype=nat.FA_F32) == nat.FA_ERR_DTYPE
+    assert dq(delta=None) == nat.FA_ERR_NULL
+    assert dq(dO=A + 4) == nat.FA_ERR_ALIGN
+    assert dq(N=0) == nat.FA_ERR_SHAPE
+    assert dkdv(D=256) == nat.FA_ERR_HEAD_DIM
+    assert dkdv(dv=None) == nat.FA_ERR_NULL
+    assert dkdv(scale=float("inf")) == nat.FA_ERR_SCALE
+    assert dkdv(lse=A + 12) == nat.FA_ERR_ALIGN
+
+
+def test_selftest_rejects_bad_limit(lib):
+    assert lib.fa_selftest_timeout(0, None) == nat.FA_ERR_SHAPE
+    assert lib.fa_selftest_timeout(3_000_000, None) == nat.FA_ERR_SHAPE
+
+
+# ----------------------------------------------------------------------------- GPU-side checks
+@pytest.mark.gpu
+def test_host_pointer_is_rejected_before_launch(lib):
+    import torch
+    from helpers import cuda_or_skip
+    dev = cuda_or_skip()
+    q = torch.randn(1, 1, 64, 64, device=dev).bfloat16()
+    host = torch.empty(1, 1, 64, 64, dtype=torch.bfloat16)  # pageable host memory
+    lse = torch.empty(1, 1, 64, device=dev)
+    rc = lib.fa_forward(q.data_ptr(), q.data_ptr(), q.data_ptr(), host.data_ptr(), lse.data_ptr(), 1, 1, 64, 64,
+                        0.125, 0, nat.FA_BF16, None)
+    assert rc == nat.FA_ERR_DEVICE_PTR
+
+
+@pytest.mark.gpu
+def test_bounded_wait_times_out_and_reports(lib):
+    """A wait on a barrier nothing arrives on ends after its limit and the status word says so;
+    the context stays usable afterwards."""
+    import torch
+    from helpers import cuda_or_skip
+    import attention_tiled_fwd_gb300 as fa
+    dev = cuda_or_skip()
+    assert fa.fa_device_status() == 0
+    fa.fa_selftest_timeout(20000)  # 20 ms
+    assert fa.fa_device_status() == nat.FA_ERR_TIMEOUT
+    assert fa.fa_device_status() == 0  # read clears it
+    x = torch.ones(1024, device=dev)
+    assert float(x.sum()) == 1024.0
