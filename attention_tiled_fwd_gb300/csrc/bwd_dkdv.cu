@@ -10,19 +10,20 @@
 //   atomics, no scratch.  Causal: only query tiles on or below the diagonal
 //   (queries >= keys) are visited.
 //
-// GB300 mapping: warp 0 TMA producer (K, V once; Q_i, dO_i through a ring),
-// warp 1 TMEM allocator + tcgen05 issuer, warps 2-5 one key row per thread
-// (L_i and D_i of the current query tile are broadcast from shared memory).
-// TMEM: S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D,256+2D).
-// P^T and dS^T (bf16) feed their MMAs as the TMEM A operand, with dO_i / Q_i
-// as MN-major B operands (queries are the reduction).
-// tcgen05.mma operations are only ordered among MMAs on the same accumulator.
-//   D = 64: P^T and dS^T get their own 64 columns each ([384,448), [448,512));
-//     the compute warps write them only after S^T_i / dP^T_i completed, and the
-//     commits behind those track dV_{i-1} / dK_{i-1}, their previous readers.
-//   D = 128: TMEM is full, so P^T is written over the first 64 columns of S^T
-//     and dS^T over the first 64 of dP^T, and the issuer waits for dV_{i-1}
-//     (resp. dK_{i-1}) to complete before S^T_i (resp. dP^T_i) overwrites them.
+// GB300 mapping: warp 0 TMA producer (K, V once; 64-row Q_i, dO_i tiles through
+// a ring), warp 1 TMEM allocator + tcgen05 issuer, warps 2-5 one key row per
+// thread (L_i and D_i of the current query tile are broadcast from shared
+// memory as float4).
+// TMEM (128 lanes = keys): S^T[b] = [64b, 64b+64), dP^T[b] = [128+64b, ...),
+// dV [256, 256+D), dK [256+D, 256+2D), b = i % 2.  The query tile is 64 rows so
+// that S^T and dP^T are double-buffered: the tensor core computes tile i+1
+// while the compute warps turn tile i into P^T and dS^T.
+// P^T (bf16) is written over the first 32 columns of S^T[b] and dS^T over the
+// first 32 of dP^T[b]; they feed dV / dK as the TMEM A operand, with dO_i / Q_i
+// as MN-major B operands (queries are the reduction).  tcgen05.mma operations
+// are only ordered among MMAs on the same accumulator, so the issuer waits for
+// dV_{i-2} (resp. dK_{i-2}) to complete before S^T_i (resp. dP^T_i) overwrites
+// that buffer; those waits are two tiles old and normally already satisfied.
 #include "fa_internal.h"
 #include "sm100_ptx.cuh"
 #include <cmath>
@@ -30,7 +31,8 @@
 namespace fa {
 namespace {
 
-constexpr int kBM = 128, kBN = 128;  // query tile, key tile
+constexpr int kBN = 128;          // keys per CTA (TMEM lanes)
+constexpr int kBQ = kDkdvQRows;   // queries per tile
 constexpr int kThreads = 192;
 
 enum : int { kSiteKV = 41, kSiteSlotEmpty, kSiteSlotFull, kSiteSFull, kSitePReady, kSiteDpFull, kSiteDsReady,
@@ -38,15 +40,16 @@ enum : int { kSiteKV = 41, kSiteSlotEmpty, kSiteSlotFull, kSiteSFull, kSitePRead
 
 template <int D, int NSLOT>
 struct DkdvSmem {
-    static constexpr int kTileBytes = kBM * D * 2;
+    static constexpr int kKVBytes = kBN * D * 2;
+    static constexpr int kTileBytes = kBQ * D * 2;  // one Q_i or dO_i tile
     static constexpr int kKOff = 0;
-    static constexpr int kVOff = kTileBytes;
-    static constexpr int kSlotOff = 2 * kTileBytes;  // slots hold Q_i, dO_i alternately
-    static constexpr int kStatOff = kSlotOff + NSLOT * kTileBytes;  // lse2[2][128], delta[2][128]
-    static constexpr int kBarOff = kStatOff + 4 * 128 * 4;
-    // kv_full, slot_full[NSLOT], slot_empty[NSLOT], s_full, p_ready, dp_full, ds_ready, final, stats[2],
-    // dv_done, dk_done
-    static constexpr int kNumBars = 1 + 2 * NSLOT + 9;
+    static constexpr int kVOff = kKVBytes;
+    static constexpr int kSlotOff = 2 * kKVBytes;
+    static constexpr int kStatOff = kSlotOff + NSLOT * kTileBytes;  // lse2[2][kBQ], delta[2][kBQ]
+    static constexpr int kBarOff = kStatOff + 4 * kBQ * 4;
+    // kv_full, slot_full[NSLOT], slot_empty[NSLOT], s_full[2], dp_full[2], p_ready[2], ds_ready[2],
+    // stats[2], dv_done, dk_done, final
+    static constexpr int kNumBars = 1 + 2 * NSLOT + 13;
     static constexpr int kTmemHolderOff = kBarOff + kNumBars * 8;
     static constexpr int kAlloc = kTmemHolderOff + 16 + 1024;
 };
@@ -59,9 +62,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     using L = DkdvSmem<D, NSLOT>;
     constexpr int kPanels = D / 64;
     constexpr uint32_t kTmemCols = 512;
-    constexpr bool kSep = 256 + 2 * D + 128 <= 512;  // room for separate P^T and dS^T buffers
-    constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
-    constexpr uint32_t kColP = kSep ? 256 + 2 * D : kColS, kColDS = kSep ? 256 + 2 * D + 64 : kColDP;
+    constexpr uint32_t kColDV = 256, kColDK = 256 + D;
     static_assert(256 + 2 * D <= 512, "TMEM budget");
 
     extern __shared__ uint8_t smem_raw[];
@@ -69,29 +70,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *k_s = smem + L::kKOff;
     uint8_t *v_s = smem + L::kVOff;
     uint8_t *slots = smem + L::kSlotOff;
-    float *lse_s = reinterpret_cast<float *>(smem + L::kStatOff);  // [2][128], already times log2(e)
-    float *del_s = lse_s + 256;                                     // [2][128]
+    float *lse_s = reinterpret_cast<float *>(smem + L::kStatOff);  // [2][kBQ], already times log2(e)
+    float *del_s = lse_s + 2 * kBQ;                                 // [2][kBQ]
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
     uint64_t *kv_full = bars;
     uint64_t *slot_full = bars + 1;
     uint64_t *slot_empty = slot_full + NSLOT;
-    uint64_t *s_full = slot_empty + NSLOT;  // S^T and dP^T of the tile issued; S^T complete
-    uint64_t *p_ready = s_full + 1;
-    uint64_t *dp_full = p_ready + 1;
-    uint64_t *ds_ready = dp_full + 1;
-    uint64_t *final_bar = ds_ready + 1;
-    uint64_t *stats_bar = final_bar + 1;  // [2]: the 128 compute threads published a stats buffer
+    uint64_t *s_full = slot_empty + NSLOT;  // [2]
+    uint64_t *dp_full = s_full + 2;         // [2]
+    uint64_t *p_ready = dp_full + 2;        // [2]
+    uint64_t *ds_ready = p_ready + 2;       // [2]
+    uint64_t *stats_bar = ds_ready + 2;     // [2]: the 128 compute threads published a stats buffer
     uint64_t *dv_done = stats_bar + 2;
     uint64_t *dk_done = dv_done + 1;
+    uint64_t *final_bar = dk_done + 1;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kTmemHolderOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int k_tile = blockIdx.x;  // causal: tile 0 has the most query tiles, launched first
     const int bh = blockIdx.z * a.H + blockIdx.y;
     const int N = a.N;
-    const int n_q_total = (N + kBM - 1) / kBM;
-    const int q_begin = a.causal ? (k_tile * kBN) / kBM : 0;
-    const int n_q = n_q_total - q_begin;
+    const int n_q_total = (N + kBQ - 1) / kBQ;
+    const int q_begin = a.causal ? (k_tile * kBN) / kBQ : 0;
+    const int n_q = n_q_total - q_begin;  // >= 1
 
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
@@ -99,15 +100,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&slot_full[s], 1);
             mbar_init(&slot_empty[s], 1);
         }
-        mbar_init(s_full, 1);
-        mbar_init(p_ready, 128);
-        mbar_init(dp_full, 1);
-        mbar_init(ds_ready, 128);
-        mbar_init(final_bar, 1);
-        mbar_init(&stats_bar[0], 128);
-        mbar_init(&stats_bar[1], 128);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&s_full[b], 1);
+            mbar_init(&dp_full[b], 1);
+            mbar_init(&p_ready[b], 128);
+            mbar_init(&ds_ready[b], 128);
+            mbar_init(&stats_bar[b], 128);
+        }
         mbar_init(dv_done, 1);
         mbar_init(dk_done, 1);
+        mbar_init(final_bar, 1);
         fence_mbarrier_init();
     }
     if (warp == 1) {
@@ -125,7 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tmap_k);
             tma_prefetch_desc(&tmap_v);
             tma_prefetch_desc(&tmap_do);
-            mbar_arrive_expect_tx(kv_full, 2 * L::kTileBytes);
+            mbar_arrive_expect_tx(kv_full, 2 * L::kKVBytes);
 #pragma unroll
             for (int p = 0; p < kPanels; ++p) {
                 tma_load_3d(k_s + p * (kBN * 128), &tmap_k, kv_full, p * 64, k_tile * kBN, bh);
@@ -142,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(&slot_full[slot], L::kTileBytes);
 #pragma unroll
                 for (int p = 0; p < kPanels; ++p)
-                    tma_load_3d(dst + p * (kBM * 128), map, &slot_full[slot], p * 64, (q_begin + (idx >> 1)) * kBM,
+                    tma_load_3d(dst + p * (kBQ * 128), map, &slot_full[slot], p * 64, (q_begin + (idx >> 1)) * kBQ,
                                 bh);
 #pragma unroll
                 for (int s = 0; s < NSLOT; ++s)
@@ -156,55 +158,67 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(kBN, kBM, false, false);  // S^T, dP^T
-            constexpr uint32_t idesc_g = idesc_bf16_f32(kBN, D, false, true);     // dV, dK
+            constexpr uint32_t idesc_s = idesc_bf16_f32(kBN, kBQ, false, false);  // S^T, dP^T: 128 x 64
+            constexpr uint32_t idesc_g = idesc_bf16_f32(kBN, D, false, true);     // dV, dK: 128 x D
             const uint32_t k_addr = smem_u32(k_s), v_addr = smem_u32(v_s), slot_addr = smem_u32(slots);
             bool ok = mbar_wait(kv_full, 0, a.status, kSiteKV);
             tc_fence_after();
-            for (int i = 0; ok && i < n_q; ++i) {
-                const int q_idx = 2 * i, q_slot = q_idx % NSLOT, q_round = q_idx / NSLOT;
-                const int d_idx = 2 * i + 1, d_slot = d_idx % NSLOT, d_round = d_idx / NSLOT;
-                if (!(ok = mbar_wait(&slot_full[q_slot], q_round & 1, a.status, kSiteSlotFull))) break;
-                if (!(ok = mbar_wait(&slot_full[d_slot], d_round & 1, a.status, kSiteSlotFull))) break;
+            // S^T_i and dP^T_i into buffer i % 2
+            auto issue_sdp = [&](int i) -> bool {
+                const int q_slot = (2 * i) % NSLOT, q_round = (2 * i) / NSLOT;
+                const int d_slot = (2 * i + 1) % NSLOT, d_round = (2 * i + 1) / NSLOT;
+                const uint32_t b = i & 1;
+                if (!mbar_wait(&slot_full[q_slot], q_round & 1, a.status, kSiteSlotFull)) return false;
+                tc_fence_after();
+                // buffer b last held P^T_{i-2}, read by dV_{i-2}
+                if (i >= 2 && !mbar_wait(dv_done, (i - 2) & 1, a.status, kSiteDvDone)) return false;
                 tc_fence_after();
                 const uint32_t qbase = slot_addr + q_slot * L::kTileBytes;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks)
+                    mma_ss(tmem + 64 * b, sdesc_sw128(k_addr + (ks >> 2) * (kBN * 128) + (ks & 3) * 32, 16, 1024),
+                           sdesc_sw128(qbase + (ks >> 2) * (kBQ * 128) + (ks & 3) * 32, 16, 1024), idesc_s, ks > 0);
+                mma_commit(&s_full[b]);
+                if (!mbar_wait(&slot_full[d_slot], d_round & 1, a.status, kSiteSlotFull)) return false;
+                tc_fence_after();
+                // buffer b last held dS^T_{i-2}, read by dK_{i-2}
+                if (i >= 2 && !mbar_wait(dk_done, (i - 2) & 1, a.status, kSiteDkDone)) return false;
+                tc_fence_after();
                 const uint32_t dbase = slot_addr + d_slot * L::kTileBytes;
-                // S^T = K Q_i^T  (its columns last held P^T_{i-1} when P^T aliases S^T)
-                if (!kSep && i > 0 && !(ok = mbar_wait(dv_done, (i - 1) & 1, a.status, kSiteDvDone))) break;
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * (kBM * 128) + (ks & 3) * 32;
-                    mma_ss(tmem + kColS, sdesc_sw128(k_addr + off, 16, 1024), sdesc_sw128(qbase + off, 16, 1024),
-                           idesc_s, ks > 0);
-                }
-                mma_commit(s_full);
-                // dP^T = V dO_i^T  (its columns last held dS^T_{i-1} when dS^T aliases dP^T)
-                if (!kSep && i > 0 && !(ok = mbar_wait(dk_done, (i - 1) & 1, a.status, kSiteDkDone))) break;
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * (kBM * 128) + (ks & 3) * 32;
-                    mma_ss(tmem + kColDP, sdesc_sw128(v_addr + off, 16, 1024), sdesc_sw128(dbase + off, 16, 1024),
-                           idesc_s, ks > 0);
-                }
-                mma_commit(dp_full);
+                for (int ks = 0; ks < D / 16; ++ks)
+                    mma_ss(tmem + 128 + 64 * b,
+                           sdesc_sw128(v_addr + (ks >> 2) * (kBN * 128) + (ks & 3) * 32, 16, 1024),
+                           sdesc_sw128(dbase + (ks >> 2) * (kBQ * 128) + (ks & 3) * 32, 16, 1024), idesc_s, ks > 0);
+                mma_commit(&dp_full[b]);
+                return true;
+            };
+            if (ok) ok = issue_sdp(0);
+            if (ok && n_q > 1) ok = issue_sdp(1);
+            for (int i = 0; ok && i < n_q; ++i) {
+                const uint32_t b = i & 1;
+                const int q_slot = (2 * i) % NSLOT, d_slot = (2 * i + 1) % NSLOT;
+                const uint32_t qbase = slot_addr + q_slot * L::kTileBytes;
+                const uint32_t dbase = slot_addr + d_slot * L::kTileBytes;
                 // dV += P^T dO_i
-                if (!(ok = mbar_wait(p_ready, i & 1, a.status, kSitePReady))) break;
+                if (!(ok = mbar_wait(&p_ready[b], (i >> 1) & 1, a.status, kSitePReady))) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kBM / 16; ++kk)
-                    mma_ts(tmem + kColDV, tmem + kColP + kk * 8, sdesc_sw128(dbase + kk * 2048, kBM * 128, 1024),
+                for (int kk = 0; kk < kBQ / 16; ++kk)
+                    mma_ts(tmem + kColDV, tmem + 64 * b + kk * 8, sdesc_sw128(dbase + kk * 2048, kBQ * 128, 1024),
                            idesc_g, (i > 0 || kk > 0));
                 mma_commit(&slot_empty[d_slot]);
                 mma_commit(dv_done);
                 // dK += dS^T Q_i
-                if (!(ok = mbar_wait(ds_ready, i & 1, a.status, kSiteDsReady))) break;
+                if (!(ok = mbar_wait(&ds_ready[b], (i >> 1) & 1, a.status, kSiteDsReady))) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kBM / 16; ++kk)
-                    mma_ts(tmem + kColDK, tmem + kColDS + kk * 8, sdesc_sw128(qbase + kk * 2048, kBM * 128, 1024),
-                           idesc_g, (i > 0 || kk > 0));
+                for (int kk = 0; kk < kBQ / 16; ++kk)
+                    mma_ts(tmem + kColDK, tmem + 128 + 64 * b + kk * 8,
+                           sdesc_sw128(qbase + kk * 2048, kBQ * 128, 1024), idesc_g, (i > 0 || kk > 0));
                 mma_commit(&slot_empty[q_slot]);
                 mma_commit(dk_done);
+                if (i + 2 < n_q) ok = issue_sdp(i + 2);
             }
             mma_commit(final_bar);
             mbar_wait(final_bar, 0, a.status, kSiteFinal);
@@ -219,92 +233,101 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float c = a.scale_log2, sc = a.scale;
         const float *lse_g = a.lse + (size_t)bh * N;
         const float *del_g = a.delta + (size_t)bh * N;
+        // threads 0..63 carry L (times log2 e) of query tid, threads 64..127 carry D of query tid - 64
+        const bool carries_lse = tid < kBQ;
+        const int stat_q = carries_lse ? tid : tid - kBQ;
+        auto load_stat = [&](int q_tile_idx) -> float {
+            const int qi = q_tile_idx * kBQ + stat_q;
+            if (carries_lse) return qi < N ? lse_g[qi] * 1.4426950408889634f : INFINITY;
+            return qi < N ? del_g[qi] : 0.f;
+        };
+        auto store_stat = [&](int buf, float v) {
+            if (carries_lse)
+                lse_s[buf * kBQ + stat_q] = v;
+            else
+                del_s[buf * kBQ + stat_q] = v;
+        };
         bool ok = true;
-        // stats of query tile q_begin into buffer 0
-        {
-            const int qi = q_begin * kBM + tid;
-            lse_s[tid] = qi < N ? lse_g[qi] * 1.4426950408889634f : INFINITY;
-            del_s[tid] = qi < N ? del_g[qi] : 0.f;
-            mbar_arrive(&stats_bar[0]);
-        }
+        store_stat(0, load_stat(q_begin));
+        mbar_arrive(&stats_bar[0]);
         for (int i = 0; i < n_q; ++i) {
             const int qt = q_begin + i;
-            const int buf = i & 1;
-            // prefetch next tile's stats into registers
-            float nl = INFINITY, nd = 0.f;
-            if (i + 1 < n_q) {
-                const int qn = (qt + 1) * kBM + tid;
-                if (qn < N) {
-                    nl = lse_g[qn] * 1.4426950408889634f;
-                    nd = del_g[qn];
-                }
-            }
-            // stats of this tile visible to all compute threads (bounded wait, no named barrier)
-            ok = mbar_wait(&stats_bar[buf], (i >> 1) & 1, a.status, kSiteStats);
+            const int b = i & 1;
+            const float nxt = (i + 1 < n_q) ? load_stat(qt + 1) : 0.f;  // prefetch; published at the end
+            ok = mbar_wait(&stats_bar[b], (i >> 1) & 1, a.status, kSiteStats);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            const float *ls = lse_s + buf * 128;
-            const float *ds = del_s + buf * 128;
-            const int q0 = qt * kBM;
-            // visible iff key <= query (causal) and query < N
-            const bool need_mask = (q0 + kBM > N) || (a.causal && key > q0) || (key >= N);
-            ok = mbar_wait(s_full, i & 1, a.status, kSiteSFull);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            tc_fence_after();
-            // P^T row as bf16 pairs: the MMA operand, and (unpacked) the factor of dS^T below.
-            uint32_t pk[kBM / 2];
+            const float4 *ls4 = reinterpret_cast<const float4 *>(lse_s + b * kBQ);
+            const float4 *ds4 = reinterpret_cast<const float4 *>(del_s + b * kBQ);
+            const int q0 = qt * kBQ;
+            // visible iff key <= query (causal), query < N and key < N
+            const bool need_mask = (q0 + kBQ > N) || (a.causal && key > q0) || (key >= N);
             const bool any_mask = __any_sync(0xffffffffu, need_mask);
-#pragma unroll
-            for (int ch = 0; ch < kBM / 32; ++ch) {
-                uint32_t raw[32];
-                tmem_ld32(tmem + lane_base + kColS + ch * 32, raw);
-                tmem_wait_ld();
-#pragma unroll
-                for (int t = 0; t < 32; t += 2) {
-                    const int qc = ch * 32 + t;
-                    float p0 = ex2_approx(fmaf(__uint_as_float(raw[t]), c, -ls[qc]));
-                    float p1 = ex2_approx(fmaf(__uint_as_float(raw[t + 1]), c, -ls[qc + 1]));
-                    if (any_mask) {
-                        const int qq = q0 + qc;
-                        if (qq >= N || key >= N || (a.causal && qq < key)) p0 = 0.f;
-                        if (qq + 1 >= N || key >= N || (a.causal && qq + 1 < key)) p1 = 0.f;
-                    }
-                    pk[qc / 2] = pack_bf16x2(p0, p1);
-                }
-            }
-#pragma unroll
-            for (int ch = 0; ch < kBM / 64; ++ch) tmem_st32(tmem + lane_base + kColP + ch * 32, pk + ch * 32);
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(p_ready);
 
-            ok = mbar_wait(dp_full, i & 1, a.status, kSiteDpFull);
+            ok = mbar_wait(&s_full[b], (i >> 1) & 1, a.status, kSiteSFull);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
-#pragma unroll
-            for (int ch = 0; ch < kBM / 32; ++ch) {
-                uint32_t raw[32], dsk[16];
-                tmem_ld32(tmem + lane_base + kColDP + ch * 32, raw);
+            // P^T row as bf16 pairs: the dV operand, and (unpacked) the factor of dS^T below.
+            uint32_t pk[kBQ / 2];
+            {
+                uint32_t raw[kBQ];
+                tmem_ld32(tmem + lane_base + 64 * b, raw);
+                tmem_ld32(tmem + lane_base + 64 * b + 32, raw + 32);
                 tmem_wait_ld();
 #pragma unroll
-                for (int t = 0; t < 32; t += 2) {
-                    const int qc = ch * 32 + t;
-                    const float2 pf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&pk[qc / 2]));
-                    const float d0 = pf.x * (__uint_as_float(raw[t]) - ds[qc]) * sc;
-                    const float d1 = pf.y * (__uint_as_float(raw[t + 1]) - ds[qc + 1]) * sc;
-                    dsk[t / 2] = pack_bf16x2(d0, d1);
+                for (int q4 = 0; q4 < kBQ / 4; ++q4) {
+                    const float4 l4 = ls4[q4];
+                    float p[4];
+                    p[0] = ex2_approx(fmaf(__uint_as_float(raw[4 * q4 + 0]), c, -l4.x));
+                    p[1] = ex2_approx(fmaf(__uint_as_float(raw[4 * q4 + 1]), c, -l4.y));
+                    p[2] = ex2_approx(fmaf(__uint_as_float(raw[4 * q4 + 2]), c, -l4.z));
+                    p[3] = ex2_approx(fmaf(__uint_as_float(raw[4 * q4 + 3]), c, -l4.w));
+                    if (any_mask) {
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            const int qq = q0 + 4 * q4 + t;
+                            if (qq >= N || key >= N || (a.causal && qq < key)) p[t] = 0.f;
+                        }
+                    }
+                    pk[2 * q4] = pack_bf16x2(p[0], p[1]);
+                    pk[2 * q4 + 1] = pack_bf16x2(p[2], p[3]);
                 }
-                // When aliased: dS^T over dP^T columns [16 ch, 16 ch + 16), already read by chunks <= ch.
-                tmem_st16(tmem + lane_base + kColDS + ch * 16, dsk);
+            }
+            tmem_st32(tmem + lane_base + 64 * b, pk);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&p_ready[b]);
+
+            ok = mbar_wait(&dp_full[b], (i >> 1) & 1, a.status, kSiteDpFull);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            tc_fence_after();
+            {
+                uint32_t raw[kBQ], dsk[kBQ / 2];
+                tmem_ld32(tmem + lane_base + 128 + 64 * b, raw);
+                tmem_ld32(tmem + lane_base + 128 + 64 * b + 32, raw + 32);
+                tmem_wait_ld();
+#pragma unroll
+                for (int q4 = 0; q4 < kBQ / 4; ++q4) {
+                    const float4 d4 = ds4[q4];
+                    const float2 p01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&pk[2 * q4]));
+                    const float2 p23 =
+                        __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&pk[2 * q4 + 1]));
+                    const float d0 = p01.x * (__uint_as_float(raw[4 * q4 + 0]) - d4.x) * sc;
+                    const float d1 = p01.y * (__uint_as_float(raw[4 * q4 + 1]) - d4.y) * sc;
+                    const float d2 = p23.x * (__uint_as_float(raw[4 * q4 + 2]) - d4.z) * sc;
+                    const float d3 = p23.y * (__uint_as_float(raw[4 * q4 + 3]) - d4.w) * sc;
+                    dsk[2 * q4] = pack_bf16x2(d0, d1);
+                    dsk[2 * q4 + 1] = pack_bf16x2(d2, d3);
+                }
+                tmem_st32(tmem + lane_base + 128 + 64 * b, dsk);
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(ds_ready);
-            // Publish the next tile's stats into the other buffer.  Its readers of two tiles ago are
-            // done: each of them arrived on this tile's stats barrier only after its last read.
+            mbar_arrive(&ds_ready[b]);
+            // Publish the next tile's stats into the other buffer.  Its readers (tile i-1) are done:
+            // every thread arrived on this tile's stats barrier only after finishing tile i-1.
             if (i + 1 < n_q) {
-                lse_s[(buf ^ 1) * 128 + tid] = nl;
-                del_s[(buf ^ 1) * 128 + tid] = nd;
-                mbar_arrive(&stats_bar[buf ^ 1]);
+                store_stat(b ^ 1, nxt);
+                mbar_arrive(&stats_bar[b ^ 1]);
             }
         }
         if (ok) {
@@ -375,8 +398,8 @@ cudaError_t launch_spec(const BwdArgs &a, const CUtensorMap &tq, const CUtensorM
 cudaError_t launch_bwd_dkdv(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             const CUtensorMap &tdo, cudaStream_t s) {
     switch (a.D) {
-        case 64: return launch_spec<64, 8>(a, tq, tk, tv, tdo, s);
-        case 128: return launch_spec<128, 4>(a, tq, tk, tv, tdo, s);
+        case 64: return launch_spec<64, 16>(a, tq, tk, tv, tdo, s);
+        case 128: return launch_spec<128, 8>(a, tq, tk, tv, tdo, s);
         default: return cudaErrorInvalidValue;
     }
 }

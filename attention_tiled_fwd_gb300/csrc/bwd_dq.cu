@@ -11,14 +11,21 @@
 //   because float atomics are emulated on its GPU; it parallelises fully over
 //   query rows here as there).
 //
-// GB300 mapping: warp 0 TMA producer (Q and dO once; K_j, V_j through a ring),
-// warp 1 TMEM allocator + tcgen05 issuer, warps 2-5 one query row per thread.
-// TMEM: S [0,128), dP [128,256), dQ [256, 256+D), dS [256+D, 320+D).  dS
-// (bf16) is fed to the dQ MMA straight from TMEM (A operand); K_j is the B
-// operand in MN-major form (keys are the reduction).  MMAs on different
-// accumulators are not ordered with each other, so dS has its own columns:
-// the compute warps write dS_j only after S_j / dP_j completed, and the commit
-// behind those tracks dQ_{j-1}, the previous reader of the dS buffer.
+// GB300 mapping: warp 0 TMA producer (Q and dO once; 64-row K_j, V_j tiles
+// through a ring), warp 1 TMEM allocator + tcgen05 issuer, warps 2-5 one query
+// row per thread.
+// TMEM (128 lanes = queries): S[b] = [64b, 64b+64), dP[b] = [128+64b, ...),
+// dQ [256, 256+D), b = j % 2, and dS[j % 3] = [256+D+32(j%3), +32).  The key
+// tile is 64 rows so that S and dP are double-buffered: the tensor core
+// computes S_{j+1}, dP_{j+1} and dQ_{j-1} while the compute warps turn tile j
+// into dS.  Issue order after dS_j is ready: S_{j+2}, dP_{j+2}, then dQ_j.
+// dS (bf16) is the TMEM A operand of dQ += dS K_j; K_j is the B operand in
+// MN-major form (keys are the reduction).  tcgen05.mma operations on different
+// accumulators are not ordered with each other, so every buffer is rewritten
+// only after its previous reader is known complete: the compute warps write
+// dS_j after S_j / dP_j completed, and the commit behind those tracks
+// dQ_{j-3}, the previous reader of dS[j % 3] (S_j is issued after dQ_{j-3}
+// and before dQ_{j-2}, hence three dS buffers).
 #include "fa_internal.h"
 #include "sm100_ptx.cuh"
 #include <cmath>
@@ -26,20 +33,22 @@
 namespace fa {
 namespace {
 
-constexpr int kBM = 128, kBN = 128;
+constexpr int kBM = 128;          // queries per CTA (TMEM lanes)
+constexpr int kBN = kDqKRows;     // keys per tile
 constexpr int kThreads = 192;
 
 enum : int { kSiteQ = 21, kSiteSlotEmpty, kSiteSlotFull, kSiteSFull, kSiteDsFull, kSiteDq, kSiteFinal, kSiteDrain };
 
 template <int D, int NSLOT>
 struct DqSmem {
-    static constexpr int kTileBytes = kBM * D * 2;  // Q, dO, K_j, V_j tiles are all 128 x D bf16
+    static constexpr int kQBytes = kBM * D * 2;     // Q and dO: 128 x D bf16 each
+    static constexpr int kTileBytes = kBN * D * 2;  // one K_j or V_j tile
     static constexpr int kQOff = 0;
-    static constexpr int kDoOff = kTileBytes;
-    static constexpr int kSlotOff = 2 * kTileBytes;
+    static constexpr int kDoOff = kQBytes;
+    static constexpr int kSlotOff = 2 * kQBytes;
     static constexpr int kBarOff = kSlotOff + NSLOT * kTileBytes;
-    // q_full, slot_full[NSLOT], slot_empty[NSLOT], s_full, ds_full, dq_done, final
-    static constexpr int kNumBars = 1 + 2 * NSLOT + 4;
+    // q_full, slot_full[NSLOT], slot_empty[NSLOT], s_full[2], ds_full[2], final
+    static constexpr int kNumBars = 1 + 2 * NSLOT + 5;
     static constexpr int kTmemHolderOff = kBarOff + kNumBars * 8;
     static constexpr int kAlloc = kTmemHolderOff + 16 + 1024;
 };
@@ -52,8 +61,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     using L = DqSmem<D, NSLOT>;
     constexpr int kPanels = D / 64;
     constexpr uint32_t kTmemCols = 512;
-    constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 256 + D;
-    static_assert(kColDS + 64 <= 512, "TMEM budget");
+    constexpr uint32_t kColDQ = 256, kColDS = 256 + D;
+    static_assert(kColDS + 96 <= 512, "TMEM budget");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -64,18 +73,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *q_full = bars;
     uint64_t *slot_full = bars + 1;
     uint64_t *slot_empty = slot_full + NSLOT;
-    uint64_t *s_full = slot_empty + NSLOT;  // S and dP of the tile are both ready
-    uint64_t *ds_full = s_full + 1;
-    uint64_t *dq_done = ds_full + 1;
-    uint64_t *final_bar = dq_done + 1;
+    uint64_t *s_full = slot_empty + NSLOT;  // [2]: S_j and dP_j complete
+    uint64_t *ds_full = s_full + 2;         // [2]: dS_j written (and S_j, dP_j read)
+    uint64_t *final_bar = ds_full + 2;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kTmemHolderOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int q_tile = gridDim.x - 1 - blockIdx.x;
+    const int q_tile = gridDim.x - 1 - blockIdx.x;  // heaviest causal tiles first
     const int bh = blockIdx.z * a.H + blockIdx.y;
     const int N = a.N;
     const int kv_end = a.causal ? min(N, (q_tile + 1) * kBM) : N;
-    const int n_kv = (kv_end + kBN - 1) / kBN;
+    const int n_kv = (kv_end + kBN - 1) / kBN;  // >= 1
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
@@ -83,9 +91,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&slot_full[s], 1);
             mbar_init(&slot_empty[s], 1);
         }
-        mbar_init(s_full, 1);
-        mbar_init(ds_full, 128);
-        mbar_init(dq_done, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&s_full[b], 1);
+            mbar_init(&ds_full[b], 128);
+        }
         mbar_init(final_bar, 1);
         fence_mbarrier_init();
     }
@@ -104,7 +113,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tmap_k);
             tma_prefetch_desc(&tmap_v);
             tma_prefetch_desc(&tmap_do);
-            mbar_arrive_expect_tx(q_full, 2 * L::kTileBytes);
+            mbar_arrive_expect_tx(q_full, 2 * L::kQBytes);
 #pragma unroll
             for (int p = 0; p < kPanels; ++p) {
                 tma_load_3d(q_s + p * (kBM * 128), &tmap_q, q_full, p * 64, q_tile * kBM, bh);
@@ -134,41 +143,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc_sq = idesc_bf16_f32(kBM, kBN, false, false);  // S, dP
-            constexpr uint32_t idesc_dq = idesc_bf16_f32(kBM, D, false, true);     // dQ += dS K
+            constexpr uint32_t idesc_sq = idesc_bf16_f32(kBM, kBN, false, false);  // S, dP: 128 x 64
+            constexpr uint32_t idesc_dq = idesc_bf16_f32(kBM, D, false, true);     // dQ += dS K: 128 x D
             const uint32_t q_addr = smem_u32(q_s), do_addr = smem_u32(do_s), slot_addr = smem_u32(slots);
             bool ok = mbar_wait(q_full, 0, a.status, kSiteQ);
             tc_fence_after();
-            for (int j = 0; ok && j < n_kv; ++j) {
-                const int ks_idx = 2 * j, k_slot = ks_idx % NSLOT, k_round = ks_idx / NSLOT;
-                const int vs_idx = 2 * j + 1, v_slot = vs_idx % NSLOT, v_round = vs_idx / NSLOT;
-                if (!(ok = mbar_wait(&slot_full[k_slot], k_round & 1, a.status, kSiteSlotFull))) break;
-                if (!(ok = mbar_wait(&slot_full[v_slot], v_round & 1, a.status, kSiteSlotFull))) break;
+            // S_j = Q K_j^T and dP_j = dO V_j^T into buffer j % 2.  The compute warps have read
+            // S_{j-2} and dP_{j-2} (ds_full of tile j-2 was waited on before this is called).
+            auto issue_sdp = [&](int j) -> bool {
+                const int k_slot = (2 * j) % NSLOT, k_round = (2 * j) / NSLOT;
+                const int v_slot = (2 * j + 1) % NSLOT, v_round = (2 * j + 1) / NSLOT;
+                const uint32_t b = j & 1;
+                if (!mbar_wait(&slot_full[k_slot], k_round & 1, a.status, kSiteSlotFull)) return false;
+                if (!mbar_wait(&slot_full[v_slot], v_round & 1, a.status, kSiteSlotFull)) return false;
                 tc_fence_after();
                 const uint32_t kbase = slot_addr + k_slot * L::kTileBytes;
                 const uint32_t vbase = slot_addr + v_slot * L::kTileBytes;
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * (kBM * 128) + (ks & 3) * 32;
-                    mma_ss(tmem + kColS, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
-                           idesc_sq, ks > 0);
-                }
+                for (int ks = 0; ks < D / 16; ++ks)
+                    mma_ss(tmem + 64 * b, sdesc_sw128(q_addr + (ks >> 2) * (kBM * 128) + (ks & 3) * 32, 16, 1024),
+                           sdesc_sw128(kbase + (ks >> 2) * (kBN * 128) + (ks & 3) * 32, 16, 1024), idesc_sq,
+                           ks > 0);
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * (kBM * 128) + (ks & 3) * 32;
-                    mma_ss(tmem + kColDP, sdesc_sw128(do_addr + off, 16, 1024), sdesc_sw128(vbase + off, 16, 1024),
-                           idesc_sq, ks > 0);
-                }
-                mma_commit(s_full);
-                mma_commit(&slot_empty[v_slot]);
-                if (!(ok = mbar_wait(ds_full, j & 1, a.status, kSiteDsFull))) break;
+                for (int ks = 0; ks < D / 16; ++ks)
+                    mma_ss(tmem + 128 + 64 * b,
+                           sdesc_sw128(do_addr + (ks >> 2) * (kBM * 128) + (ks & 3) * 32, 16, 1024),
+                           sdesc_sw128(vbase + (ks >> 2) * (kBN * 128) + (ks & 3) * 32, 16, 1024), idesc_sq,
+                           ks > 0);
+                mma_commit(&s_full[b]);
+                mma_commit(&slot_empty[v_slot]);  // V_j is no longer needed
+                return true;
+            };
+            if (ok) ok = issue_sdp(0);
+            if (ok && n_kv > 1) ok = issue_sdp(1);
+            for (int j = 0; ok && j < n_kv; ++j) {
+                const uint32_t b = j & 1;
+                const int k_slot = (2 * j) % NSLOT;
+                const uint32_t kbase = slot_addr + k_slot * L::kTileBytes;
+                if (!(ok = mbar_wait(&ds_full[b], (j >> 1) & 1, a.status, kSiteDsFull))) break;
                 tc_fence_after();
+                // S[b], dP[b] are free again: queue tile j+2 first so the compute warps never wait on dQ_j.
+                if (j + 2 < n_kv && !(ok = issue_sdp(j + 2))) break;
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)
-                    mma_ts(tmem + kColDQ, tmem + kColDS + kk * 8, sdesc_sw128(kbase + kk * 2048, kBN * 128, 1024),
-                           idesc_dq, (j > 0 || kk > 0));
+                    mma_ts(tmem + kColDQ, tmem + kColDS + 32 * (j % 3) + kk * 8,
+                           sdesc_sw128(kbase + kk * 2048, kBN * 128, 1024), idesc_dq, (j > 0 || kk > 0));
                 mma_commit(&slot_empty[k_slot]);
-                mma_commit(dq_done);
             }
             mma_commit(final_bar);
             mbar_wait(final_bar, 0, a.status, kSiteFinal);
@@ -205,40 +225,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P = 2^(S c - L log2 e); invalid rows get P = 0.
         const float lse2 = valid ? a.lse[(size_t)bh * N + row] * 1.4426950408889634f : INFINITY;
         const float sc = a.scale;
+        const int lim = a.causal ? min(N - 1, row) : N - 1;  // last visible key
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
-            ok = mbar_wait(s_full, j & 1, a.status, kSiteSFull);
+            const uint32_t b = j & 1;
+            ok = mbar_wait(&s_full[b], (j >> 1) & 1, a.status, kSiteSFull);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
             const int key0 = j * kBN;
             const bool need_mask = (key0 + kBN > N) || (a.causal && key0 + kBN - 1 > q_tile * kBM);
-            const int lim = a.causal ? min(N - 1, row) : N - 1;
+            uint32_t sraw[kBN], praw[kBN], dsk[kBN / 2];
+            tmem_ld32(tmem + lane_base + 64 * b, sraw);
+            tmem_ld32(tmem + lane_base + 64 * b + 32, sraw + 32);
+            tmem_ld32(tmem + lane_base + 128 + 64 * b, praw);
+            tmem_ld32(tmem + lane_base + 128 + 64 * b + 32, praw + 32);
+            tmem_wait_ld();
 #pragma unroll
-            for (int ch = 0; ch < kBN / 32; ++ch) {
-                uint32_t sraw[32], praw[32], dsk[16];
-                tmem_ld32(tmem + lane_base + kColS + ch * 32, sraw);
-                tmem_ld32(tmem + lane_base + kColDP + ch * 32, praw);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    float p0 = ex2_approx(fmaf(__uint_as_float(sraw[i]), c, -lse2));
-                    float p1 = ex2_approx(fmaf(__uint_as_float(sraw[i + 1]), c, -lse2));
-                    if (need_mask) {
-                        if (key0 + ch * 32 + i > lim) p0 = 0.f;
-                        if (key0 + ch * 32 + i + 1 > lim) p1 = 0.f;
-                    }
-                    const float ds0 = p0 * (__uint_as_float(praw[i]) - delta) * sc;
-                    const float ds1 = p1 * (__uint_as_float(praw[i + 1]) - delta) * sc;
-                    dsk[i / 2] = pack_bf16x2(ds0, ds1);
+            for (int i = 0; i < kBN; i += 2) {
+                float p0 = ex2_approx(fmaf(__uint_as_float(sraw[i]), c, -lse2));
+                float p1 = ex2_approx(fmaf(__uint_as_float(sraw[i + 1]), c, -lse2));
+                if (need_mask) {
+                    if (key0 + i > lim) p0 = 0.f;
+                    if (key0 + i + 1 > lim) p1 = 0.f;
                 }
-                tmem_st16(tmem + lane_base + kColDS + ch * 16, dsk);
+                const float ds0 = p0 * (__uint_as_float(praw[i]) - delta) * sc;
+                const float ds1 = p1 * (__uint_as_float(praw[i + 1]) - delta) * sc;
+                dsk[i / 2] = pack_bf16x2(ds0, ds1);
             }
+            tmem_st32(tmem + lane_base + kColDS + 32 * (j % 3), dsk);
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(ds_full);
+            mbar_arrive(&ds_full[b]);
         }
         if (ok) {
-            ok = mbar_wait(dq_done, (n_kv - 1) & 1, a.status, kSiteDq);
+            ok = mbar_wait(final_bar, 0, a.status, kSiteDq);  // single phase: every MMA has completed
             ok = __all_sync(0xffffffffu, ok);
         }
         if (ok) {
@@ -300,8 +320,8 @@ cudaError_t launch_spec(const BwdArgs &a, const CUtensorMap &tq, const CUtensorM
 cudaError_t launch_bwd_dq(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                           const CUtensorMap &tdo, cudaStream_t s) {
     switch (a.D) {
-        case 64: return launch_spec<64, 8>(a, tq, tk, tv, tdo, s);
-        case 128: return launch_spec<128, 4>(a, tq, tk, tv, tdo, s);
+        case 64: return launch_spec<64, 16>(a, tq, tk, tv, tdo, s);
+        case 128: return launch_spec<128, 8>(a, tq, tk, tv, tdo, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -20,6 +20,10 @@ constexpr FwdSpec kFwdSpecs[] = {
     {256, 128, 64, 4},   // Q 64 KB + 4 x 32 KB ring; TMEM 2x64 + 256 (D-blocked O)
 };
 
+// Tile rows of the backward kernels' streamed operands (TMA box heights).
+constexpr int kDqKRows = 64;    // dQ kernel: 128 query rows per CTA, 64-key K/V tiles
+constexpr int kDkdvQRows = 64;  // dK/dV kernel: 128 keys per CTA, 64-query Q/dO tiles
+
 struct FwdArgs {
     const void *q, *k, *v;
     void *o;

@@ -275,7 +275,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&p_full[j & 1]);
         }
         if (ok) {
-            ok = mbar_wait(pv_done, (n_kv - 1) & 1, a.status, kSitePV);
+            // O is final once every MMA has completed: final_bar has a single phase, committed by the
+            // issuer after its last MMA.  (Waiting on pv_done's parity here would be ambiguous: only
+            // PV_{n-3} is known to be complete at this point, so pv_done may be two phases behind.)
+            ok = mbar_wait(final_bar, 0, a.status, kSiteFinal);
             ok = __all_sync(0xffffffffu, ok);
         }
         if (ok) {

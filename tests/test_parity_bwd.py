@@ -57,6 +57,21 @@ def test_backward_small_shapes(shape, causal, grad_dtype):
     assert_close(to_np(g["lse"]), ref["lse"], TOL_LSE, what="lse")
 
 
+@pytest.mark.parametrize("shape", [(1, 2, 1100, 64), (1, 2, 900, 128)])
+def test_backward_repeated_many_tiles(shape):
+    """Many tiles per CTA in both backward kernels, several runs (pipeline-race check)."""
+    dev = cuda_or_skip()
+    B, H, N, D = shape
+    inp = make_qkv(B, H, N, D, seed=400 + N + D, dtype="bf16", with_dO=True)
+    scale = 1.0 / np.sqrt(D)
+    for causal in (False, True):
+        ref = oracle.backward(inp["q"], inp["k"], inp["v"], inp["dO"], scale, causal)
+        for rep in range(3):
+            g = _fwd_bwd(inp, causal, dev, scale, torch.float32)
+            for n in ("dq", "dk", "dv"):
+                assert_close(to_np(g[n]), ref[n], TOL_BF16, what=f"{n} rep {rep} causal={causal}")
+
+
 def test_backward_invariants_hold_on_gpu():
     """Column sums: sum_j dK_j = 0 (rows of dS sum to 0) and sum_j dV_j = sum_i dO_i."""
     dev = cuda_or_skip()

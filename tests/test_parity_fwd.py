@@ -95,6 +95,22 @@ def test_bf16_forward_increasing_logits_force_rescale():
         assert_close(to_np(lse), rl, TOL_LSE, what="bf16 LSE rising max")
 
 
+@pytest.mark.parametrize("shape", [(1, 2, 320, 256), (2, 2, 448, 256), (1, 4, 1000, 64), (1, 2, 1152, 128)])
+def test_bf16_forward_repeated_many_tiles(shape):
+    """Many K/V tiles per CTA, non-causal and causal, several runs: catches pipeline races whose
+    outcome depends on the relative speed of the MMA issuer and the softmax warps."""
+    dev = cuda_or_skip()
+    B, H, N, D = shape
+    inp = make_qkv(B, H, N, D, seed=300 + N + D, dtype="bf16")
+    scale = 1.0 / np.sqrt(D)
+    for causal in (False, True):
+        ro, rl = oracle.forward(inp["q"], inp["k"], inp["v"], scale, causal)
+        for rep in range(4):
+            o, lse = _run_fwd(inp, causal, dev, scale)
+            assert_close(to_np(o), ro, TOL_BF16, BF16_REL, what=f"bf16 O rep {rep} causal={causal}")
+            assert_close(to_np(lse), rl, TOL_LSE, what=f"bf16 LSE rep {rep}")
+
+
 def test_bf16_forward_is_deterministic():
     dev = cuda_or_skip()
     inp = make_qkv(2, 2, 1000, 128, seed=3, dtype="bf16")
