@@ -11,16 +11,21 @@
 //   (queries >= keys) are visited.
 //
 // GB300 mapping: warp 0 TMA producer (K, V once; 64-row Q_i, dO_i tiles through
-// a ring), warp 1 TMEM allocator + tcgen05 issuer, warps 2-5 one key row per
-// thread (L_i and D_i of the current query tile are broadcast from shared
-// memory as float4).
+// a ring), warp 1 TMEM allocator + tcgen05 issuer, warps 2-9 compute: two
+// warpgroups, each thread owning one key row (its TMEM lane) and one half (32
+// queries) of every tile's columns -- P^T and dS^T are elementwise given the
+// queries' L_i and D_i (broadcast from shared memory as float4), so the halves
+// never exchange data, and two warps per SM sub-partition hide latencies.
 // TMEM (128 lanes = keys): S^T[b] = [64b, 64b+64), dP^T[b] = [128+64b, ...),
 // dV [256, 256+D), dK [256+D, 256+2D), b = i % 2.  The query tile is 64 rows so
 // that S^T and dP^T are double-buffered: the tensor core computes tile i+1
 // while the compute warps turn tile i into P^T and dS^T.
-// P^T (bf16) is written over the first 32 columns of S^T[b] and dS^T over the
-// first 32 of dP^T[b]; they feed dV / dK as the TMEM A operand, with dO_i / Q_i
-// as MN-major B operands (queries are the reduction).  tcgen05.mma operations
+// P^T (bf16) overwrites S^T[b] and dS^T overwrites dP^T[b]: each warpgroup
+// packs its 32 queries into the first 16 columns of its own 32-column half
+// (columns [32g, 32g+16)), so neither half writes columns the other has yet
+// to read.  They feed dV / dK as the TMEM A operand (16-query step kk reads
+// columns 32(kk/2) + 8(kk%2)), with dO_i / Q_i as MN-major B operands (queries
+// are the reduction).  tcgen05.mma operations
 // are only ordered among MMAs on the same accumulator, so the issuer waits for
 // dV_{i-2} (resp. dK_{i-2}) to complete before S^T_i (resp. dP^T_i) overwrites
 // that buffer; those waits are two tiles old and normally already satisfied.
@@ -33,7 +38,8 @@ namespace {
 
 constexpr int kBN = 128;          // keys per CTA (TMEM lanes)
 constexpr int kBQ = kDkdvQRows;   // queries per tile
-constexpr int kThreads = 192;
+constexpr int kComputeWG = 2;     // compute warpgroups, one column half each
+constexpr int kThreads = 64 + 128 * kComputeWG;
 
 enum : int { kSiteKV = 41, kSiteSlotEmpty, kSiteSlotFull, kSiteSFull, kSitePReady, kSiteDpFull, kSiteDsReady,
              kSiteDone, kSiteFinal, kSiteDrain, kSiteStats, kSiteDvDone, kSiteDkDone };
@@ -80,7 +86,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *dp_full = s_full + 2;         // [2]
     uint64_t *p_ready = dp_full + 2;        // [2]
     uint64_t *ds_ready = p_ready + 2;       // [2]
-    uint64_t *stats_bar = ds_ready + 2;     // [2]: the 128 compute threads published a stats buffer
+    uint64_t *stats_bar = ds_ready + 2;     // [2]: all compute threads are done with / published a stats buffer
     uint64_t *dv_done = stats_bar + 2;
     uint64_t *dk_done = dv_done + 1;
     uint64_t *final_bar = dk_done + 1;
@@ -103,9 +109,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(&s_full[b], 1);
             mbar_init(&dp_full[b], 1);
-            mbar_init(&p_ready[b], 128);
-            mbar_init(&ds_ready[b], 128);
-            mbar_init(&stats_bar[b], 128);
+            mbar_init(&p_ready[b], 128 * kComputeWG);
+            mbar_init(&ds_ready[b], 128 * kComputeWG);
+            mbar_init(&stats_bar[b], 128 * kComputeWG);
         }
         mbar_init(dv_done, 1);
         mbar_init(dk_done, 1);
@@ -157,91 +163,109 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(kBN, kBQ, false, false);  // S^T, dP^T: 128 x 64
-            constexpr uint32_t idesc_g = idesc_bf16_f32(kBN, D, false, true);     // dV, dK: 128 x D
-            const uint32_t k_addr = smem_u32(k_s), v_addr = smem_u32(v_s), slot_addr = smem_u32(slots);
-            bool ok = mbar_wait(kv_full, 0, a.status, kSiteKV);
+        // MMA issuer: the whole warp runs the loop, one elected lane issues MMAs and their commits.
+        constexpr uint32_t idesc_s = idesc_bf16_f32(kBN, kBQ, false, false);  // S^T, dP^T: 128 x 64
+        constexpr uint32_t idesc_g = idesc_bf16_f32(kBN, D, false, true);     // dV, dK: 128 x D
+        const uint64_t k_desc = sdesc_sw128(smem_u32(k_s), 16, 1024);
+        const uint64_t v_desc = sdesc_sw128(smem_u32(v_s), 16, 1024);
+        const uint32_t slot_addr = smem_u32(slots);
+        const bool leader = elect_one();
+        bool ok = warp_wait(kv_full, 0, a.status, kSiteKV);
+        tc_fence_after();
+        // S^T_i and dP^T_i into buffer i % 2
+        auto issue_sdp = [&](int i) -> bool {
+            const int q_slot = (2 * i) % NSLOT, q_round = (2 * i) / NSLOT;
+            const int d_slot = (2 * i + 1) % NSLOT, d_round = (2 * i + 1) / NSLOT;
+            const uint32_t b = i & 1;
+            if (!warp_wait(&slot_full[q_slot], q_round & 1, a.status, kSiteSlotFull)) return false;
+            // buffer b last held P^T_{i-2}, read by dV_{i-2}
+            if (i >= 2 && !warp_wait(dv_done, (i - 2) & 1, a.status, kSiteDvDone)) return false;
             tc_fence_after();
-            // S^T_i and dP^T_i into buffer i % 2
-            auto issue_sdp = [&](int i) -> bool {
-                const int q_slot = (2 * i) % NSLOT, q_round = (2 * i) / NSLOT;
-                const int d_slot = (2 * i + 1) % NSLOT, d_round = (2 * i + 1) / NSLOT;
-                const uint32_t b = i & 1;
-                if (!mbar_wait(&slot_full[q_slot], q_round & 1, a.status, kSiteSlotFull)) return false;
-                tc_fence_after();
-                // buffer b last held P^T_{i-2}, read by dV_{i-2}
-                if (i >= 2 && !mbar_wait(dv_done, (i - 2) & 1, a.status, kSiteDvDone)) return false;
-                tc_fence_after();
-                const uint32_t qbase = slot_addr + q_slot * L::kTileBytes;
+            const uint64_t q_desc = sdesc_sw128(slot_addr + q_slot * L::kTileBytes, 16, 1024);
+            if (leader) {
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
-                    mma_ss(tmem + 64 * b, sdesc_sw128(k_addr + (ks >> 2) * (kBN * 128) + (ks & 3) * 32, 16, 1024),
-                           sdesc_sw128(qbase + (ks >> 2) * (kBQ * 128) + (ks & 3) * 32, 16, 1024), idesc_s, ks > 0);
+                    mma_ss(tmem + 64 * b, sdesc_add(k_desc, (ks >> 2) * (kBN * 128) + (ks & 3) * 32),
+                           sdesc_add(q_desc, (ks >> 2) * (kBQ * 128) + (ks & 3) * 32), idesc_s, ks > 0);
                 mma_commit(&s_full[b]);
-                if (!mbar_wait(&slot_full[d_slot], d_round & 1, a.status, kSiteSlotFull)) return false;
-                tc_fence_after();
-                // buffer b last held dS^T_{i-2}, read by dK_{i-2}
-                if (i >= 2 && !mbar_wait(dk_done, (i - 2) & 1, a.status, kSiteDkDone)) return false;
-                tc_fence_after();
-                const uint32_t dbase = slot_addr + d_slot * L::kTileBytes;
+            }
+            __syncwarp();
+            if (!warp_wait(&slot_full[d_slot], d_round & 1, a.status, kSiteSlotFull)) return false;
+            // buffer b last held dS^T_{i-2}, read by dK_{i-2}
+            if (i >= 2 && !warp_wait(dk_done, (i - 2) & 1, a.status, kSiteDkDone)) return false;
+            tc_fence_after();
+            const uint64_t do_desc = sdesc_sw128(slot_addr + d_slot * L::kTileBytes, 16, 1024);
+            if (leader) {
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
-                    mma_ss(tmem + 128 + 64 * b,
-                           sdesc_sw128(v_addr + (ks >> 2) * (kBN * 128) + (ks & 3) * 32, 16, 1024),
-                           sdesc_sw128(dbase + (ks >> 2) * (kBQ * 128) + (ks & 3) * 32, 16, 1024), idesc_s, ks > 0);
+                    mma_ss(tmem + 128 + 64 * b, sdesc_add(v_desc, (ks >> 2) * (kBN * 128) + (ks & 3) * 32),
+                           sdesc_add(do_desc, (ks >> 2) * (kBQ * 128) + (ks & 3) * 32), idesc_s, ks > 0);
                 mma_commit(&dp_full[b]);
-                return true;
-            };
-            if (ok) ok = issue_sdp(0);
-            if (ok && n_q > 1) ok = issue_sdp(1);
-            for (int i = 0; ok && i < n_q; ++i) {
-                const uint32_t b = i & 1;
-                const int q_slot = (2 * i) % NSLOT, d_slot = (2 * i + 1) % NSLOT;
-                const uint32_t qbase = slot_addr + q_slot * L::kTileBytes;
-                const uint32_t dbase = slot_addr + d_slot * L::kTileBytes;
-                // dV += P^T dO_i
-                if (!(ok = mbar_wait(&p_ready[b], (i >> 1) & 1, a.status, kSitePReady))) break;
-                tc_fence_after();
+            }
+            __syncwarp();
+            return true;
+        };
+        if (ok) ok = issue_sdp(0);
+        if (ok && n_q > 1) ok = issue_sdp(1);
+        for (int i = 0; ok && i < n_q; ++i) {
+            const uint32_t b = i & 1;
+            const int q_slot = (2 * i) % NSLOT, d_slot = (2 * i + 1) % NSLOT;
+            const uint64_t qmn_desc = sdesc_sw128(slot_addr + q_slot * L::kTileBytes, kBQ * 128, 1024);
+            const uint64_t dmn_desc = sdesc_sw128(slot_addr + d_slot * L::kTileBytes, kBQ * 128, 1024);
+            // dV += P^T dO_i
+            if (!(ok = warp_wait(&p_ready[b], (i >> 1) & 1, a.status, kSitePReady))) break;
+            tc_fence_after();
+            if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < kBQ / 16; ++kk)
-                    mma_ts(tmem + kColDV, tmem + 64 * b + kk * 8, sdesc_sw128(dbase + kk * 2048, kBQ * 128, 1024),
-                           idesc_g, (i > 0 || kk > 0));
+                    mma_ts(tmem + kColDV, tmem + 64 * b + (kk >> 1) * 32 + (kk & 1) * 8,
+                           sdesc_add(dmn_desc, kk * 2048), idesc_g, (i > 0 || kk > 0));
                 mma_commit(&slot_empty[d_slot]);
                 mma_commit(dv_done);
-                // dK += dS^T Q_i
-                if (!(ok = mbar_wait(&ds_ready[b], (i >> 1) & 1, a.status, kSiteDsReady))) break;
-                tc_fence_after();
+            }
+            __syncwarp();
+            // dK += dS^T Q_i
+            if (!(ok = warp_wait(&ds_ready[b], (i >> 1) & 1, a.status, kSiteDsReady))) break;
+            tc_fence_after();
+            if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < kBQ / 16; ++kk)
-                    mma_ts(tmem + kColDK, tmem + 128 + 64 * b + kk * 8,
-                           sdesc_sw128(qbase + kk * 2048, kBQ * 128, 1024), idesc_g, (i > 0 || kk > 0));
+                    mma_ts(tmem + kColDK, tmem + 128 + 64 * b + (kk >> 1) * 32 + (kk & 1) * 8,
+                           sdesc_add(qmn_desc, kk * 2048), idesc_g, (i > 0 || kk > 0));
                 mma_commit(&slot_empty[q_slot]);
                 mma_commit(dk_done);
-                if (i + 2 < n_q) ok = issue_sdp(i + 2);
             }
-            mma_commit(final_bar);
-            mbar_wait(final_bar, 0, a.status, kSiteFinal);
+            __syncwarp();
+            if (i + 2 < n_q) ok = issue_sdp(i + 2);
         }
+        if (leader) mma_commit(final_bar);
         __syncwarp();
+        warp_wait(final_bar, 0, a.status, kSiteFinal);
     } else {
         const int quarter = warp & 3;
-        const int tid = (warp - 2) * 32 + lane;  // 0..127 for the stats loads
+        const int g = (warp - 2) >> 2;           // column (query) half of every tile
+        const int tid = (warp - 2) * 32 + lane;  // 0..255; 0..127 load the stats
         const int r = quarter * 32 + lane;       // key row within the tile (TMEM lane)
         const int key = k_tile * kBN + r;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         const float c = a.scale_log2, sc = a.scale;
         const float *lse_g = a.lse + (size_t)bh * N;
         const float *del_g = a.delta + (size_t)bh * N;
-        // threads 0..63 carry L (times log2 e) of query tid, threads 64..127 carry D of query tid - 64
+        constexpr int kHalf = kBQ / kComputeWG;  // 32 queries per thread per tile
+        // threads 0..63 carry L (times log2 e) of query tid, threads 64..127 carry D of query tid - 64;
+        // every compute thread arrives on the stats barrier (so a buffer is rewritten only after all
+        // 256 threads finished reading it)
+        const bool carries = tid < 2 * kBQ;
         const bool carries_lse = tid < kBQ;
         const int stat_q = carries_lse ? tid : tid - kBQ;
         auto load_stat = [&](int q_tile_idx) -> float {
+            if (!carries) return 0.f;
             const int qi = q_tile_idx * kBQ + stat_q;
             if (carries_lse) return qi < N ? lse_g[qi] * 1.4426950408889634f : INFINITY;
             return qi < N ? del_g[qi] : 0.f;
         };
         auto store_stat = [&](int buf, float v) {
+            if (!carries) return;
             if (carries_lse)
                 lse_s[buf * kBQ + stat_q] = v;
             else
@@ -256,25 +280,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float nxt = (i + 1 < n_q) ? load_stat(qt + 1) : 0.f;  // prefetch; published at the end
             ok = mbar_wait(&stats_bar[b], (i >> 1) & 1, a.status, kSiteStats);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            const float4 *ls4 = reinterpret_cast<const float4 *>(lse_s + b * kBQ);
-            const float4 *ds4 = reinterpret_cast<const float4 *>(del_s + b * kBQ);
-            const int q0 = qt * kBQ;
+            const float4 *ls4 = reinterpret_cast<const float4 *>(lse_s + b * kBQ + g * kHalf);
+            const float4 *ds4 = reinterpret_cast<const float4 *>(del_s + b * kBQ + g * kHalf);
+            const int q0 = qt * kBQ + g * kHalf;  // first query of this thread's half
             // visible iff key <= query (causal), query < N and key < N
-            const bool need_mask = (q0 + kBQ > N) || (a.causal && key > q0) || (key >= N);
+            const bool need_mask = (q0 + kHalf > N) || (a.causal && key > q0) || (key >= N);
             const bool any_mask = __any_sync(0xffffffffu, need_mask);
 
             ok = mbar_wait(&s_full[b], (i >> 1) & 1, a.status, kSiteSFull);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
-            // P^T row as bf16 pairs: the dV operand, and (unpacked) the factor of dS^T below.
-            uint32_t pk[kBQ / 2];
+            // P^T row half as bf16 pairs: the dV operand, and (unpacked) the factor of dS^T below.
+            uint32_t pk[kHalf / 2];
             {
-                uint32_t raw[kBQ];
-                tmem_ld32(tmem + lane_base + 64 * b, raw);
-                tmem_ld32(tmem + lane_base + 64 * b + 32, raw + 32);
+                uint32_t raw[kHalf];
+                tmem_ld32(tmem + lane_base + 64 * b + g * kHalf, raw);
                 tmem_wait_ld();
 #pragma unroll
-                for (int q4 = 0; q4 < kBQ / 4; ++q4) {
+                for (int q4 = 0; q4 < kHalf / 4; ++q4) {
                     const float4 l4 = ls4[q4];
                     float p[4];
                     p[0] = ex2_approx(fmaf(__uint_as_float(raw[4 * q4 + 0]), c, -l4.x));
@@ -292,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pk[2 * q4 + 1] = pack_bf16x2(p[2], p[3]);
                 }
             }
-            tmem_st32(tmem + lane_base + 64 * b, pk);
+            tmem_st16(tmem + lane_base + 64 * b + g * kHalf, pk);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&p_ready[b]);
@@ -301,12 +324,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
             {
-                uint32_t raw[kBQ], dsk[kBQ / 2];
-                tmem_ld32(tmem + lane_base + 128 + 64 * b, raw);
-                tmem_ld32(tmem + lane_base + 128 + 64 * b + 32, raw + 32);
+                uint32_t raw[kHalf], dsk[kHalf / 2];
+                tmem_ld32(tmem + lane_base + 128 + 64 * b + g * kHalf, raw);
                 tmem_wait_ld();
 #pragma unroll
-                for (int q4 = 0; q4 < kBQ / 4; ++q4) {
+                for (int q4 = 0; q4 < kHalf / 4; ++q4) {
                     const float4 d4 = ds4[q4];
                     const float2 p01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&pk[2 * q4]));
                     const float2 p23 =
@@ -318,13 +340,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dsk[2 * q4] = pack_bf16x2(d0, d1);
                     dsk[2 * q4 + 1] = pack_bf16x2(d2, d3);
                 }
-                tmem_st32(tmem + lane_base + 128 + 64 * b, dsk);
+                tmem_st16(tmem + lane_base + 128 + 64 * b + g * kHalf, dsk);
             }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&ds_ready[b]);
             // Publish the next tile's stats into the other buffer.  Its readers (tile i-1) are done:
-            // every thread arrived on this tile's stats barrier only after finishing tile i-1.
+            // every compute thread arrived on this tile's stats barrier only after finishing tile i-1.
             if (i + 1 < n_q) {
                 store_stat(b ^ 1, nxt);
                 mbar_arrive(&stats_bar[b ^ 1]);
@@ -337,36 +359,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
             tc_fence_after();
             const bool valid = key < N;
+            // warpgroup 0 writes dV, warpgroup 1 writes dK
+            const uint32_t col = g == 0 ? kColDV : kColDK;
+            void *outp = g == 0 ? a.dv : a.dk;
+            uint32_t v[32];
 #pragma unroll
-            for (int which = 0; which < 2; ++which) {
-                const uint32_t col = which == 0 ? kColDV : kColDK;
-                void *outp = which == 0 ? a.dv : a.dk;
-                uint32_t v[32];
+            for (int ch = 0; ch < D / 32; ++ch) {
+                tmem_ld32(tmem + lane_base + col + ch * 32, v);
+                tmem_wait_ld();
+                if (!valid) continue;
+                if (a.grad_bf16) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(outp) +
+                                                           ((size_t)bh * N + key) * D + ch * 32);
 #pragma unroll
-                for (int ch = 0; ch < D / 32; ++ch) {
-                    tmem_ld32(tmem + lane_base + col + ch * 32, v);
-                    tmem_wait_ld();
-                    if (!valid) continue;
-                    if (a.grad_bf16) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(outp) +
-                                                               ((size_t)bh * N + key) * D + ch * 32);
-#pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4) {
-                            uint4 w;
-                            w.x = pack_bf16x2(__uint_as_float(v[v4 * 8 + 0]), __uint_as_float(v[v4 * 8 + 1]));
-                            w.y = pack_bf16x2(__uint_as_float(v[v4 * 8 + 2]), __uint_as_float(v[v4 * 8 + 3]));
-                            w.z = pack_bf16x2(__uint_as_float(v[v4 * 8 + 4]), __uint_as_float(v[v4 * 8 + 5]));
-                            w.w = pack_bf16x2(__uint_as_float(v[v4 * 8 + 6]), __uint_as_float(v[v4 * 8 + 7]));
-                            dst[v4] = w;
-                        }
-                    } else {
-                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(outp) +
-                                                                 ((size_t)bh * N + key) * D + ch * 32);
-#pragma unroll
-                        for (int v4 = 0; v4 < 8; ++v4)
-                            dst[v4] = make_float4(__uint_as_float(v[v4 * 4 + 0]), __uint_as_float(v[v4 * 4 + 1]),
-                                                  __uint_as_float(v[v4 * 4 + 2]), __uint_as_float(v[v4 * 4 + 3]));
+                    for (int v4 = 0; v4 < 4; ++v4) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(v[v4 * 8 + 0]), __uint_as_float(v[v4 * 8 + 1]));
+                        w.y = pack_bf16x2(__uint_as_float(v[v4 * 8 + 2]), __uint_as_float(v[v4 * 8 + 3]));
+                        w.z = pack_bf16x2(__uint_as_float(v[v4 * 8 + 4]), __uint_as_float(v[v4 * 8 + 5]));
+                        w.w = pack_bf16x2(__uint_as_float(v[v4 * 8 + 6]), __uint_as_float(v[v4 * 8 + 7]));
+                        dst[v4] = w;
                     }
+                } else {
+                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(outp) +
+                                                             ((size_t)bh * N + key) * D + ch * 32);
+#pragma unroll
+                    for (int v4 = 0; v4 < 8; ++v4)
+                        dst[v4] = make_float4(__uint_as_float(v[v4 * 4 + 0]), __uint_as_float(v[v4 * 4 + 1]),
+                                              __uint_as_float(v[v4 * 4 + 2]), __uint_as_float(v[v4 * 4 + 3]));
                 }
             }
         }

@@ -12,8 +12,11 @@
 //   query rows here as there).
 //
 // GB300 mapping: warp 0 TMA producer (Q and dO once; 64-row K_j, V_j tiles
-// through a ring), warp 1 TMEM allocator + tcgen05 issuer, warps 2-5 one query
-// row per thread.
+// through a ring), warp 1 TMEM allocator + tcgen05 issuer, warps 2-9 compute:
+// two warpgroups, each thread owning one query row (its TMEM lane) and one
+// half (32 keys) of every tile's columns -- dS is elementwise given the row's
+// L and D, so the halves never exchange data, and two warps per SM
+// sub-partition hide each other's latencies.
 // TMEM (128 lanes = queries): S[b] = [64b, 64b+64), dP[b] = [128+64b, ...),
 // dQ [256, 256+D), b = j % 2, and dS[j % 3] = [256+D+32(j%3), +32).  The key
 // tile is 64 rows so that S and dP are double-buffered: the tensor core
@@ -35,7 +38,8 @@ namespace {
 
 constexpr int kBM = 128;          // queries per CTA (TMEM lanes)
 constexpr int kBN = kDqKRows;     // keys per tile
-constexpr int kThreads = 192;
+constexpr int kComputeWG = 2;     // compute warpgroups, one column half each
+constexpr int kThreads = 64 + 128 * kComputeWG;
 
 enum : int { kSiteQ = 21, kSiteSlotEmpty, kSiteSlotFull, kSiteSFull, kSiteDsFull, kSiteDq, kSiteFinal, kSiteDrain };
 
@@ -93,7 +97,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&s_full[b], 1);
-            mbar_init(&ds_full[b], 128);
+            mbar_init(&ds_full[b], 128 * kComputeWG);
         }
         mbar_init(final_bar, 1);
         fence_mbarrier_init();
@@ -142,66 +146,72 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) {
-            constexpr uint32_t idesc_sq = idesc_bf16_f32(kBM, kBN, false, false);  // S, dP: 128 x 64
-            constexpr uint32_t idesc_dq = idesc_bf16_f32(kBM, D, false, true);     // dQ += dS K: 128 x D
-            const uint32_t q_addr = smem_u32(q_s), do_addr = smem_u32(do_s), slot_addr = smem_u32(slots);
-            bool ok = mbar_wait(q_full, 0, a.status, kSiteQ);
+        // MMA issuer: the whole warp runs the loop, one elected lane issues MMAs and their commits.
+        constexpr uint32_t idesc_sq = idesc_bf16_f32(kBM, kBN, false, false);  // S, dP: 128 x 64
+        constexpr uint32_t idesc_dq = idesc_bf16_f32(kBM, D, false, true);     // dQ += dS K: 128 x D
+        const uint64_t q_desc = sdesc_sw128(smem_u32(q_s), 16, 1024);
+        const uint64_t do_desc = sdesc_sw128(smem_u32(do_s), 16, 1024);
+        const uint32_t slot_addr = smem_u32(slots);
+        const bool leader = elect_one();
+        bool ok = warp_wait(q_full, 0, a.status, kSiteQ);
+        tc_fence_after();
+        // S_j = Q K_j^T and dP_j = dO V_j^T into buffer j % 2.  The compute warps have read
+        // S_{j-2} and dP_{j-2} (ds_full of tile j-2 was waited on before this is called).
+        auto issue_sdp = [&](int j) -> bool {
+            const int k_slot = (2 * j) % NSLOT, k_round = (2 * j) / NSLOT;
+            const int v_slot = (2 * j + 1) % NSLOT, v_round = (2 * j + 1) / NSLOT;
+            const uint32_t b = j & 1;
+            if (!warp_wait(&slot_full[k_slot], k_round & 1, a.status, kSiteSlotFull)) return false;
+            if (!warp_wait(&slot_full[v_slot], v_round & 1, a.status, kSiteSlotFull)) return false;
             tc_fence_after();
-            // S_j = Q K_j^T and dP_j = dO V_j^T into buffer j % 2.  The compute warps have read
-            // S_{j-2} and dP_{j-2} (ds_full of tile j-2 was waited on before this is called).
-            auto issue_sdp = [&](int j) -> bool {
-                const int k_slot = (2 * j) % NSLOT, k_round = (2 * j) / NSLOT;
-                const int v_slot = (2 * j + 1) % NSLOT, v_round = (2 * j + 1) / NSLOT;
-                const uint32_t b = j & 1;
-                if (!mbar_wait(&slot_full[k_slot], k_round & 1, a.status, kSiteSlotFull)) return false;
-                if (!mbar_wait(&slot_full[v_slot], v_round & 1, a.status, kSiteSlotFull)) return false;
-                tc_fence_after();
-                const uint32_t kbase = slot_addr + k_slot * L::kTileBytes;
-                const uint32_t vbase = slot_addr + v_slot * L::kTileBytes;
+            const uint64_t k_desc = sdesc_sw128(slot_addr + k_slot * L::kTileBytes, 16, 1024);
+            const uint64_t v_desc = sdesc_sw128(slot_addr + v_slot * L::kTileBytes, 16, 1024);
+            if (leader) {
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
-                    mma_ss(tmem + 64 * b, sdesc_sw128(q_addr + (ks >> 2) * (kBM * 128) + (ks & 3) * 32, 16, 1024),
-                           sdesc_sw128(kbase + (ks >> 2) * (kBN * 128) + (ks & 3) * 32, 16, 1024), idesc_sq,
-                           ks > 0);
+                    mma_ss(tmem + 64 * b, sdesc_add(q_desc, (ks >> 2) * (kBM * 128) + (ks & 3) * 32),
+                           sdesc_add(k_desc, (ks >> 2) * (kBN * 128) + (ks & 3) * 32), idesc_sq, ks > 0);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
-                    mma_ss(tmem + 128 + 64 * b,
-                           sdesc_sw128(do_addr + (ks >> 2) * (kBM * 128) + (ks & 3) * 32, 16, 1024),
-                           sdesc_sw128(vbase + (ks >> 2) * (kBN * 128) + (ks & 3) * 32, 16, 1024), idesc_sq,
-                           ks > 0);
+                    mma_ss(tmem + 128 + 64 * b, sdesc_add(do_desc, (ks >> 2) * (kBM * 128) + (ks & 3) * 32),
+                           sdesc_add(v_desc, (ks >> 2) * (kBN * 128) + (ks & 3) * 32), idesc_sq, ks > 0);
                 mma_commit(&s_full[b]);
                 mma_commit(&slot_empty[v_slot]);  // V_j is no longer needed
-                return true;
-            };
-            if (ok) ok = issue_sdp(0);
-            if (ok && n_kv > 1) ok = issue_sdp(1);
-            for (int j = 0; ok && j < n_kv; ++j) {
-                const uint32_t b = j & 1;
-                const int k_slot = (2 * j) % NSLOT;
-                const uint32_t kbase = slot_addr + k_slot * L::kTileBytes;
-                if (!(ok = mbar_wait(&ds_full[b], (j >> 1) & 1, a.status, kSiteDsFull))) break;
-                tc_fence_after();
-                // S[b], dP[b] are free again: queue tile j+2 first so the compute warps never wait on dQ_j.
-                if (j + 2 < n_kv && !(ok = issue_sdp(j + 2))) break;
+            }
+            __syncwarp();
+            return true;
+        };
+        if (ok) ok = issue_sdp(0);
+        if (ok && n_kv > 1) ok = issue_sdp(1);
+        for (int j = 0; ok && j < n_kv; ++j) {
+            const uint32_t b = j & 1;
+            const int k_slot = (2 * j) % NSLOT;
+            const uint64_t kmn_desc = sdesc_sw128(slot_addr + k_slot * L::kTileBytes, kBN * 128, 1024);
+            if (!(ok = warp_wait(&ds_full[b], (j >> 1) & 1, a.status, kSiteDsFull))) break;
+            tc_fence_after();
+            // S[b], dP[b] are free again: queue tile j+2 first so the compute warps never wait on dQ_j.
+            if (j + 2 < n_kv && !(ok = issue_sdp(j + 2))) break;
+            if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)
-                    mma_ts(tmem + kColDQ, tmem + kColDS + 32 * (j % 3) + kk * 8,
-                           sdesc_sw128(kbase + kk * 2048, kBN * 128, 1024), idesc_dq, (j > 0 || kk > 0));
+                    mma_ts(tmem + kColDQ, tmem + kColDS + 32 * (j % 3) + kk * 8, sdesc_add(kmn_desc, kk * 2048),
+                           idesc_dq, (j > 0 || kk > 0));
                 mma_commit(&slot_empty[k_slot]);
             }
-            mma_commit(final_bar);
-            mbar_wait(final_bar, 0, a.status, kSiteFinal);
+            __syncwarp();
         }
+        if (leader) mma_commit(final_bar);
         __syncwarp();
+        warp_wait(final_bar, 0, a.status, kSiteFinal);
     } else {
         const int quarter = warp & 3;
+        const int g = (warp - 2) >> 2;  // column half of every tile
         const int r = quarter * 32 + lane;
         const int row = q_tile * kBM + r;
         const bool valid = row < N;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         const float c = a.scale_log2;
-        // D_i = sum_d dO_id O_id for this thread's row.
+        // D_i = sum_d dO_id O_id for this thread's row (both halves compute it; half 0 stores it).
         float delta = 0.f;
         if (valid) {
             const uint4 *orow = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.o) +
@@ -220,28 +230,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     delta = fmaf(of.y, df.y, delta);
                 }
             }
-            a.delta[(size_t)bh * N + row] = delta;
+            if (g == 0) a.delta[(size_t)bh * N + row] = delta;
         }
         // P = 2^(S c - L log2 e); invalid rows get P = 0.
         const float lse2 = valid ? a.lse[(size_t)bh * N + row] * 1.4426950408889634f : INFINITY;
         const float sc = a.scale;
         const int lim = a.causal ? min(N - 1, row) : N - 1;  // last visible key
+        constexpr int kHalf = kBN / kComputeWG;              // 32 columns per thread per tile
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
             const uint32_t b = j & 1;
             ok = mbar_wait(&s_full[b], (j >> 1) & 1, a.status, kSiteSFull);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
-            const int key0 = j * kBN;
-            const bool need_mask = (key0 + kBN > N) || (a.causal && key0 + kBN - 1 > q_tile * kBM);
-            uint32_t sraw[kBN], praw[kBN], dsk[kBN / 2];
-            tmem_ld32(tmem + lane_base + 64 * b, sraw);
-            tmem_ld32(tmem + lane_base + 64 * b + 32, sraw + 32);
-            tmem_ld32(tmem + lane_base + 128 + 64 * b, praw);
-            tmem_ld32(tmem + lane_base + 128 + 64 * b + 32, praw + 32);
+            const int key0 = j * kBN + g * kHalf;
+            const bool need_mask = (key0 + kHalf > N) || (a.causal && key0 + kHalf - 1 > q_tile * kBM);
+            uint32_t sraw[kHalf], praw[kHalf], dsk[kHalf / 2];
+            tmem_ld32(tmem + lane_base + 64 * b + g * kHalf, sraw);
+            tmem_ld32(tmem + lane_base + 128 + 64 * b + g * kHalf, praw);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < kBN; i += 2) {
+            for (int i = 0; i < kHalf; i += 2) {
                 float p0 = ex2_approx(fmaf(__uint_as_float(sraw[i]), c, -lse2));
                 float p1 = ex2_approx(fmaf(__uint_as_float(sraw[i + 1]), c, -lse2));
                 if (need_mask) {
@@ -252,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float ds1 = p1 * (__uint_as_float(praw[i + 1]) - delta) * sc;
                 dsk[i / 2] = pack_bf16x2(ds0, ds1);
             }
-            tmem_st32(tmem + lane_base + kColDS + 32 * (j % 3), dsk);
+            tmem_st16(tmem + lane_base + kColDS + 32 * (j % 3) + g * (kHalf / 2), dsk);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&ds_full[b]);
@@ -265,13 +274,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             uint32_t v[32];
 #pragma unroll
-            for (int ch = 0; ch < D / 32; ++ch) {
-                tmem_ld32(tmem + lane_base + kColDQ + ch * 32, v);
+            for (int ch = 0; ch < D / 64; ++ch) {  // this half's D/2 columns of dQ
+                const int col = g * (D / 2) + ch * 32;
+                tmem_ld32(tmem + lane_base + kColDQ + col, v);
                 tmem_wait_ld();
                 if (valid) {
                     if (a.grad_bf16) {
                         uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.dq) +
-                                                               ((size_t)bh * N + row) * D + ch * 32);
+                                                               ((size_t)bh * N + row) * D + col);
 #pragma unroll
                         for (int v4 = 0; v4 < 4; ++v4) {
                             uint4 w;
@@ -283,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     } else {
                         float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.dq) +
-                                                                 ((size_t)bh * N + row) * D + ch * 32);
+                                                                 ((size_t)bh * N + row) * D + col);
 #pragma unroll
                         for (int v4 = 0; v4 < 8; ++v4)
                             dst[v4] = make_float4(__uint_as_float(v[v4 * 4 + 0]), __uint_as_float(v[v4 * 4 + 1]),

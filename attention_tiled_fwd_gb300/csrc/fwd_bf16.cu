@@ -16,8 +16,13 @@
 //                 S_j = Q K_j^T  (SS: both operands in shared memory) into one
 //                 of two S buffers in TMEM, then O += P_j V_j (TS: P_j, bf16, in
 //                 one of two P buffers in TMEM)
-//   warps 2-5   softmax: thread t owns query row t (TMEM lane t), so the row
-//               max / sum are thread-local; P is written back to TMEM as bf16.
+//   warps 2-9   softmax, two warpgroups: a thread owns one query row (its TMEM
+//               lane) and one half of every S tile's columns.  The row max is
+//               thread-local within a half; the two halves of a row combine
+//               their maxima through shared memory (one bounded mbarrier
+//               round per tile) so both use the same reference max, and add
+//               their partial sums once at the end.  P is written back to TMEM
+//               as bf16; each half rescales and normalises its half of O.
 //               The O correction is lazy: O is rescaled only when the running
 //               max grows by more than 2^8 (the "branch-guarded correction"
 //               of the metalworking page), otherwise the stale max is kept;
@@ -39,10 +44,12 @@ namespace fa {
 namespace {
 
 constexpr int kBM = 128;
-constexpr int kThreads = 192;
+constexpr int kSoftmaxWG = 2;  // softmax warpgroups, one column half each
+constexpr int kThreads = 64 + 128 * kSoftmaxWG;
 
 // Wait-site ids recorded in the status word on a time-out.
-enum : int { kSiteQ = 1, kSiteSlotEmpty, kSiteSlotFull, kSiteSFull, kSitePFull, kSitePV, kSiteFinal, kSiteDrain };
+enum : int { kSiteQ = 1, kSiteSlotEmpty, kSiteSlotFull, kSiteSFull, kSitePFull, kSitePV, kSiteFinal, kSiteDrain,
+             kSiteXchg };
 
 template <int D, int BN, int NSLOT>
 struct FwdSmem {
@@ -51,9 +58,10 @@ struct FwdSmem {
     static constexpr int kSlotBytes = BN * D * 2;
     static constexpr int kQOff = 0;
     static constexpr int kSlotOff = kQBytes;
-    static constexpr int kBarOff = kSlotOff + NSLOT * kSlotBytes;
-    // barriers: q_full, slot_full[NSLOT], slot_empty[NSLOT], s_full[2], p_full[2], pv_done, final
-    static constexpr int kNumBars = 1 + 2 * NSLOT + 2 + 2 + 1 + 1;
+    static constexpr int kXchgOff = kSlotOff + NSLOT * kSlotBytes;  // row-max exchange [2][2][128] + l [2][128]
+    static constexpr int kBarOff = kXchgOff + (4 * kBM + 2 * kBM) * 4;
+    // barriers: q_full, slot_full[NSLOT], slot_empty[NSLOT], s_full[2], p_full[2], pv_done, final, xchg[2], lx
+    static constexpr int kNumBars = 1 + 2 * NSLOT + 2 + 2 + 1 + 1 + 3;
     static constexpr int kTmemHolderOff = kBarOff + kNumBars * 8;
     static constexpr int kBytes = kTmemHolderOff + 16;
     static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment of the base
@@ -81,6 +89,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *p_full = s_full + 2;
     uint64_t *pv_done = p_full + 2;
     uint64_t *final_bar = pv_done + 1;
+    uint64_t *xchg = final_bar + 1;  // [2]: every softmax thread published its half-row max of a tile
+    uint64_t *lx = xchg + 2;         // every softmax thread published its partial row sum
+    float *smax = reinterpret_cast<float *>(smem + L::kXchgOff);  // [tile parity][half][row]
+    float *lsum = smax + 4 * kBM;                                  // [half][row]
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kTmemHolderOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -98,10 +110,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&s_full[b], 1);
-            mbar_init(&p_full[b], 128);
+            mbar_init(&p_full[b], 128 * kSoftmaxWG);
+            mbar_init(&xchg[b], 128 * kSoftmaxWG);
         }
         mbar_init(pv_done, 1);
         mbar_init(final_bar, 1);
+        mbar_init(lx, 128 * kSoftmaxWG);
         fence_mbarrier_init();
     }
     if (warp == 1) {
@@ -148,57 +162,64 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, BN, false, false);
-            constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, false, true);
-            const uint32_t q_addr = smem_u32(q_s);
-            const uint32_t slot_addr = smem_u32(slots);
-            bool ok = mbar_wait(q_full, 0, a.status, kSiteQ);
+        // The whole warp runs the loop (operands stay warp-uniform); one elected lane issues the MMAs
+        // and the commits that track them.
+        constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, BN, false, false);
+        constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, false, true);
+        const uint64_t q_desc = sdesc_sw128(smem_u32(q_s), 16, 1024);
+        const uint32_t slot_addr = smem_u32(slots);
+        const bool leader = elect_one();
+        bool ok = warp_wait(q_full, 0, a.status, kSiteQ);
+        tc_fence_after();
+        auto issue_s = [&](int j) -> bool {
+            const int idx = 2 * j, slot = idx % NSLOT, round = idx / NSLOT;
+            if (!warp_wait(&slot_full[slot], round & 1, a.status, kSiteSlotFull)) return false;
             tc_fence_after();
-            auto issue_s = [&](int j) -> bool {
-                const int idx = 2 * j, slot = idx % NSLOT, round = idx / NSLOT;
-                if (!mbar_wait(&slot_full[slot], round & 1, a.status, kSiteSlotFull)) return false;
-                tc_fence_after();
-                const uint32_t kbase = slot_addr + slot * L::kSlotBytes;
-                const uint32_t d_s = tmem + ((j & 1) ? kColS1 : kColS0);
+            const uint64_t k_desc = sdesc_sw128(slot_addr + slot * L::kSlotBytes, 16, 1024);
+            const uint32_t d_s = tmem + ((j & 1) ? kColS1 : kColS0);
+            if (leader) {
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t off = (ks & 3) * 32;  // 16 bf16 = 32 B step inside the 128-B row
-                    const uint64_t ad = sdesc_sw128(q_addr + (ks >> 2) * (kBM * 128) + off, 16, 1024);
-                    const uint64_t bd = sdesc_sw128(kbase + (ks >> 2) * (BN * 128) + off, 16, 1024);
-                    mma_ss(d_s, ad, bd, idesc_s, ks > 0);
+                    mma_ss(d_s, sdesc_add(q_desc, (ks >> 2) * (kBM * 128) + off),
+                           sdesc_add(k_desc, (ks >> 2) * (BN * 128) + off), idesc_s, ks > 0);
                 }
                 mma_commit(&s_full[j & 1]);
                 mma_commit(&slot_empty[slot]);
-                return true;
-            };
-            if (ok) ok = issue_s(0);
-            if (ok && n_kv > 1) ok = issue_s(1);
-            for (int j = 0; ok && j < n_kv; ++j) {
-                if (!(ok = mbar_wait(&p_full[j & 1], (j >> 1) & 1, a.status, kSitePFull))) break;
-                tc_fence_after();
-                const int idx = 2 * j + 1, slot = idx % NSLOT, round = idx / NSLOT;
-                if (!(ok = mbar_wait(&slot_full[slot], round & 1, a.status, kSiteSlotFull))) break;
-                tc_fence_after();
-                const uint32_t vbase = slot_addr + slot * L::kSlotBytes;
-                const uint32_t p_t = tmem + ((j & 1) ? kColP1 : kColP0);
+            }
+            __syncwarp();
+            return true;
+        };
+        if (ok) ok = issue_s(0);
+        if (ok && n_kv > 1) ok = issue_s(1);
+        for (int j = 0; ok && j < n_kv; ++j) {
+            if (!(ok = warp_wait(&p_full[j & 1], (j >> 1) & 1, a.status, kSitePFull))) break;
+            tc_fence_after();
+            const int idx = 2 * j + 1, slot = idx % NSLOT, round = idx / NSLOT;
+            if (!(ok = warp_wait(&slot_full[slot], round & 1, a.status, kSiteSlotFull))) break;
+            tc_fence_after();
+            const uint64_t v_desc = sdesc_sw128(slot_addr + slot * L::kSlotBytes, BN * 128, 1024);
+            const uint32_t p_t = tmem + ((j & 1) ? kColP1 : kColP0);
+            if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t bd = sdesc_sw128(vbase + kk * 2048, BN * 128, 1024);
-                    mma_ts(tmem + kColO, p_t + kk * 8, bd, idesc_o, (j > 0 || kk > 0));
-                }
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_ts(tmem + kColO, p_t + kk * 8, sdesc_add(v_desc, kk * 2048), idesc_o, (j > 0 || kk > 0));
                 mma_commit(&slot_empty[slot]);
                 mma_commit(pv_done);
-                if (j + 2 < n_kv) ok = issue_s(j + 2);
             }
-            // Every MMA issued above has completed before TMEM is released.
-            mma_commit(final_bar);
-            mbar_wait(final_bar, 0, a.status, kSiteFinal);
+            __syncwarp();
+            if (j + 2 < n_kv) ok = issue_s(j + 2);
         }
+        // Every MMA issued above has completed before TMEM is released.
+        if (leader) mma_commit(final_bar);
         __syncwarp();
+        warp_wait(final_bar, 0, a.status, kSiteFinal);
     } else {
         // ------------------------------------------------------------ softmax / correction / epilogue
-        const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
+        constexpr int HB = BN / kSoftmaxWG;  // S columns per thread per tile
+        constexpr int HD = D / kSoftmaxWG;   // O columns per thread
+        const int quarter = warp & 3;        // TMEM lanes [32*quarter, 32*quarter + 32)
+        const int g = (warp - 2) >> 2;       // column half
         const int r = quarter * 32 + lane;
         const int row = q_tile * kBM + r;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
@@ -206,33 +227,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
-            const uint32_t s_col = (j & 1) ? kColS1 : kColS0;
-            const uint32_t p_col = (j & 1) ? kColP1 : kColP0;
+            const uint32_t s_col = ((j & 1) ? kColS1 : kColS0) + g * HB;
+            const uint32_t p_col = ((j & 1) ? kColP1 : kColP0) + g * (HB / 2);
             ok = mbar_wait(&s_full[j & 1], (j >> 1) & 1, a.status, kSiteSFull);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
-            float s[BN];
+            float s[HB];
             {
                 uint32_t raw[32];
 #pragma unroll
-                for (int ch = 0; ch < BN / 32; ++ch) {
+                for (int ch = 0; ch < HB / 32; ++ch) {
                     tmem_ld32(tmem + lane_base + s_col + ch * 32, raw);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) s[ch * 32 + i] = __uint_as_float(raw[i]) * c;
                 }
             }
-            const int key0 = j * BN;
-            const bool need_mask = (key0 + BN > N) || (a.causal && key0 + BN - 1 > q_tile * kBM);
+            const int key0 = j * BN + g * HB;
+            const bool need_mask = (key0 + HB > N) || (a.causal && key0 + HB - 1 > q_tile * kBM);
             if (need_mask) {
                 const int lim = a.causal ? min(N - 1, row) : N - 1;  // last visible key
 #pragma unroll
-                for (int i = 0; i < BN; ++i)
+                for (int i = 0; i < HB; ++i)
                     if (key0 + i > lim) s[i] = -INFINITY;
             }
             float mt = s[0];
 #pragma unroll
-            for (int i = 1; i < BN; ++i) mt = fmaxf(mt, s[i]);
+            for (int i = 1; i < HB; ++i) mt = fmaxf(mt, s[i]);
+            // combine with the other half of the row
+            smax[((j & 1) * 2 + g) * kBM + r] = mt;
+            mbar_arrive(&xchg[j & 1]);
+            ok = mbar_wait(&xchg[j & 1], (j >> 1) & 1, a.status, kSiteXchg);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            mt = fmaxf(mt, smax[((j & 1) * 2 + (g ^ 1)) * kBM + r]);
             const float m_new = fmaxf(m, mt);
             // Lazy correction: keep the stale max unless the row max grew by > 8 (factor 256).
             const bool need = m_new > m + 8.f;
@@ -240,34 +267,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float m_base = (m_use == -INFINITY) ? 0.f : m_use;
             const float alpha = need ? ex2_approx(m - m_base) : 1.f;
             float rs = 0.f;
-            // P = 2^(S - m) as bf16 pairs into this tile's P buffer.
+            // P = 2^(S - m) as bf16 pairs into this tile's P buffer (this half's columns).
+            constexpr int kPk = HB >= 64 ? 32 : HB / 2;  // packed pairs per store (32 or 16 columns)
 #pragma unroll
-            for (int ch = 0; ch < BN / 64; ++ch) {
-                uint32_t pk[32];
+            for (int ch = 0; ch < HB / (2 * kPk); ++ch) {
+                uint32_t pk[kPk];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
+                for (int i = 0; i < kPk; ++i) {
                     const float p0 = ex2_approx(s[ch * 64 + 2 * i] - m_base);
                     const float p1 = ex2_approx(s[ch * 64 + 2 * i + 1] - m_base);
                     rs += p0 + p1;
                     pk[i] = pack_bf16x2(p0, p1);
                 }
-                tmem_st32(tmem + lane_base + p_col + ch * 32, pk);
+                if constexpr (kPk == 32)
+                    tmem_st32(tmem + lane_base + p_col + ch * 32, pk);
+                else
+                    tmem_st16(tmem + lane_base + p_col + ch * 32, pk);
             }
             l = l * alpha + rs;
             m = m_use;
             if (j > 0 && __any_sync(0xffffffffu, need)) {
-                // O must hold P_{j-1} V_{j-1} before it is rescaled.
+                // O must hold P_{j-1} V_{j-1} before it is rescaled (this half's columns).
                 ok = mbar_wait(pv_done, (j - 1) & 1, a.status, kSitePV);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc_fence_after();
                 uint32_t ov[32];
 #pragma unroll
-                for (int ch = 0; ch < D / 32; ++ch) {
-                    tmem_ld32(tmem + lane_base + kColO + ch * 32, ov);
+                for (int ch = 0; ch < HD / 32; ++ch) {
+                    const uint32_t oc = kColO + g * HD + ch * 32;
+                    tmem_ld32(tmem + lane_base + oc, ov);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                    tmem_st32(tmem + lane_base + kColO + ch * 32, ov);
+                    tmem_st32(tmem + lane_base + oc, ov);
                 }
             }
             tmem_wait_st();
@@ -282,13 +314,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __all_sync(0xffffffffu, ok);
         }
         if (ok) {
+            lsum[g * kBM + r] = l;
+            mbar_arrive(lx);
+            ok = mbar_wait(lx, 0, a.status, kSiteXchg);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        if (ok) {
+            const float l_row = l + lsum[(g ^ 1) * kBM + r];
             tc_fence_after();
-            const float inv_l = 1.f / l;
-            __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.o) + ((size_t)bh * N + row) * D;
+            const float inv_l = 1.f / l_row;
+            __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.o) + ((size_t)bh * N + row) * D + g * HD;
             uint32_t ov[32];
 #pragma unroll
-            for (int ch = 0; ch < D / 32; ++ch) {
-                tmem_ld32(tmem + lane_base + kColO + ch * 32, ov);
+            for (int ch = 0; ch < HD / 32; ++ch) {
+                tmem_ld32(tmem + lane_base + kColO + g * HD + ch * 32, ov);
                 tmem_wait_ld();
                 if (row < N) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + ch * 32);
@@ -303,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (row < N) a.lse[(size_t)bh * N + row] = (m + __log2f(l)) * 0.69314718055994531f;
+            if (row < N && g == 0) a.lse[(size_t)bh * N + row] = (m + __log2f(l_row)) * 0.69314718055994531f;
         }
     }
 

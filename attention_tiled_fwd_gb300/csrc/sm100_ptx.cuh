@@ -18,9 +18,6 @@ constexpr uint64_t kWaitLimitNs = 1500000000ull;  // 1.5 s
 
 // Status-word layout: low 16 bits = fa_status code (negative, stored as
 // its absolute value), high 16 bits = wait-site id of the first failure.
-struct KernelStatus {
-    int *word;
-};
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
@@ -83,6 +80,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *s
             return false;
         }
     }
+}
+
+// Whole-warp bounded wait: every lane waits, and the warp agrees on the outcome
+// (so warp-collective code after it stays convergent).
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int *status, int site) {
+    const bool ok = mbar_wait(bar, parity, status, site);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// One lane of a fully active warp is elected (the same lane every time for a
+// given warp state); the MMA issuers compute every operand warp-uniformly and
+// let only the elected lane issue, which keeps those operands in uniform
+// registers.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.b32 %0, 1, 0, P;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
 }
 
 // ---------------------------------------------------------------- TMA
@@ -168,6 +184,11 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr, uint32_t lbo
     return (uint64_t)((smem_addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16) |
            ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
+
+// Advance a descriptor's start address by byte_off bytes (a multiple of 16).  The
+// address field is the low 14 bits of (addr >> 4); shared-memory offsets stay
+// below 256 KB, so the add never carries into the neighbouring fields.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t byte_off) { return desc + (byte_off >> 4); }
 
 // TMEM loads/stores, 32 data-path lanes x 32-bit, one lane (row) per thread.
 #define FA_TMEM_LD_X16(taddr, r)                                                                         \
