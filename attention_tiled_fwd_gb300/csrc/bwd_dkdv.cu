@@ -11,7 +11,10 @@
 //   (queries >= keys) are visited.
 //
 // GB300 mapping: warp 0 TMA producer (K, V once; 64-row Q_i, dO_i tiles through
-// a ring), warp 1 TMEM allocator + tcgen05 issuer, warps 2-9 compute: two
+// a ring); two tcgen05 issuer warps, warp 1 (also the TMEM allocator) for
+// S^T and dP^T and warp 2 for dV and dK, so that one keeps the tensor core
+// fed while the other waits on a barrier (an MMA's issue blocks until the
+// tensor core accepts it, at its execution rate); warps 3-10 compute: two
 // warpgroups, each thread owning one key row (its TMEM lane) and one half (32
 // queries) of every tile's columns -- P^T and dS^T are elementwise given the
 // queries' L_i and D_i (broadcast from shared memory as float4), so the halves
@@ -26,9 +29,12 @@
 // to read.  They feed dV / dK as the TMEM A operand (16-query step kk reads
 // columns 32(kk/2) + 8(kk%2)), with dO_i / Q_i as MN-major B operands (queries
 // are the reduction).  tcgen05.mma operations
-// are only ordered among MMAs on the same accumulator, so the issuer waits for
-// dV_{i-2} (resp. dK_{i-2}) to complete before S^T_i (resp. dP^T_i) overwrites
-// that buffer; those waits are two tiles old and normally already satisfied.
+// are only ordered among MMAs on the same accumulator (and a commit only tracks
+// its own thread's MMAs), so the S^T/dP^T issuer waits for dV_{i-2} (resp.
+// dK_{i-2}) to complete before S^T_i (resp. dP^T_i) overwrites that buffer;
+// those waits are two tiles old and normally already satisfied.  Q_i and dO_i
+// slots are released after dK_i, which is issued only after the compute warps
+// saw S^T_i and dP^T_i complete.
 #include "fa_internal.h"
 #include "sm100_ptx.cuh"
 #include <cmath>
@@ -39,7 +45,8 @@ namespace {
 constexpr int kBN = 128;          // keys per CTA (TMEM lanes)
 constexpr int kBQ = kDkdvQRows;   // queries per tile
 constexpr int kComputeWG = 2;     // compute warpgroups, one column half each
-constexpr int kThreads = 64 + 128 * kComputeWG;
+constexpr int kFirstComputeWarp = 3;
+constexpr int kThreads = 32 * kFirstComputeWarp + 128 * kComputeWG;
 
 enum : int { kSiteKV = 41, kSiteSlotEmpty, kSiteSlotFull, kSiteSFull, kSitePReady, kSiteDpFull, kSiteDsReady,
              kSiteDone, kSiteFinal, kSiteDrain, kSiteStats, kSiteDvDone, kSiteDkDone };
@@ -54,8 +61,8 @@ struct DkdvSmem {
     static constexpr int kStatOff = kSlotOff + NSLOT * kTileBytes;  // lse2[2][kBQ], delta[2][kBQ]
     static constexpr int kBarOff = kStatOff + 4 * kBQ * 4;
     // kv_full, slot_full[NSLOT], slot_empty[NSLOT], s_full[2], dp_full[2], p_ready[2], ds_ready[2],
-    // stats[2], dv_done, dk_done, final
-    static constexpr int kNumBars = 1 + 2 * NSLOT + 13;
+    // stats[2], dv_done, dk_done, final, a_final
+    static constexpr int kNumBars = 1 + 2 * NSLOT + 14;
     static constexpr int kTmemHolderOff = kBarOff + kNumBars * 8;
     static constexpr int kAlloc = kTmemHolderOff + 16 + 1024;
 };
@@ -89,7 +96,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *stats_bar = ds_ready + 2;     // [2]: all compute threads are done with / published a stats buffer
     uint64_t *dv_done = stats_bar + 2;
     uint64_t *dk_done = dv_done + 1;
-    uint64_t *final_bar = dk_done + 1;
+    uint64_t *final_bar = dk_done + 1;   // issuer B: every dV / dK MMA has completed
+    uint64_t *a_final = final_bar + 1;   // issuer A: every S^T / dP^T MMA has completed
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kTmemHolderOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -116,6 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(dv_done, 1);
         mbar_init(dk_done, 1);
         mbar_init(final_bar, 1);
+        mbar_init(a_final, 1);
         fence_mbarrier_init();
     }
     if (warp == 1) {
@@ -163,23 +172,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        // MMA issuer: the whole warp runs the loop, one elected lane issues MMAs and their commits.
+        // Issuer A: S^T_i = K Q_i^T and dP^T_i = V dO_i^T into buffer i % 2.  The whole warp runs the
+        // loop (operands stay warp-uniform); one elected lane issues the MMAs and their commits.
         constexpr uint32_t idesc_s = idesc_bf16_f32(kBN, kBQ, false, false);  // S^T, dP^T: 128 x 64
-        constexpr uint32_t idesc_g = idesc_bf16_f32(kBN, D, false, true);     // dV, dK: 128 x D
         const uint64_t k_desc = sdesc_sw128(smem_u32(k_s), 16, 1024);
         const uint64_t v_desc = sdesc_sw128(smem_u32(v_s), 16, 1024);
         const uint32_t slot_addr = smem_u32(slots);
         const bool leader = elect_one();
         bool ok = warp_wait(kv_full, 0, a.status, kSiteKV);
         tc_fence_after();
-        // S^T_i and dP^T_i into buffer i % 2
-        auto issue_sdp = [&](int i) -> bool {
+        for (int i = 0; ok && i < n_q; ++i) {
             const int q_slot = (2 * i) % NSLOT, q_round = (2 * i) / NSLOT;
             const int d_slot = (2 * i + 1) % NSLOT, d_round = (2 * i + 1) / NSLOT;
             const uint32_t b = i & 1;
-            if (!warp_wait(&slot_full[q_slot], q_round & 1, a.status, kSiteSlotFull)) return false;
+            if (!(ok = warp_wait(&slot_full[q_slot], q_round & 1, a.status, kSiteSlotFull))) break;
             // buffer b last held P^T_{i-2}, read by dV_{i-2}
-            if (i >= 2 && !warp_wait(dv_done, (i - 2) & 1, a.status, kSiteDvDone)) return false;
+            if (i >= 2 && !(ok = warp_wait(dv_done, (i - 2) & 1, a.status, kSiteDvDone))) break;
             tc_fence_after();
             const uint64_t q_desc = sdesc_sw128(slot_addr + q_slot * L::kTileBytes, 16, 1024);
             if (leader) {
@@ -190,9 +198,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(&s_full[b]);
             }
             __syncwarp();
-            if (!warp_wait(&slot_full[d_slot], d_round & 1, a.status, kSiteSlotFull)) return false;
+            if (!(ok = warp_wait(&slot_full[d_slot], d_round & 1, a.status, kSiteSlotFull))) break;
             // buffer b last held dS^T_{i-2}, read by dK_{i-2}
-            if (i >= 2 && !warp_wait(dk_done, (i - 2) & 1, a.status, kSiteDkDone)) return false;
+            if (i >= 2 && !(ok = warp_wait(dk_done, (i - 2) & 1, a.status, kSiteDkDone))) break;
             tc_fence_after();
             const uint64_t do_desc = sdesc_sw128(slot_addr + d_slot * L::kTileBytes, 16, 1024);
             if (leader) {
@@ -203,16 +211,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(&dp_full[b]);
             }
             __syncwarp();
-            return true;
-        };
-        if (ok) ok = issue_sdp(0);
-        if (ok && n_q > 1) ok = issue_sdp(1);
+        }
+        // Drain this warp's MMAs before TMEM can be released (immediate in the normal path).
+        if (leader) mma_commit(a_final);
+        __syncwarp();
+        warp_wait(a_final, 0, a.status, kSiteFinal);
+    } else if (warp == 2) {
+        // Issuer B: dV += P^T dO_i and dK += dS^T Q_i.
+        constexpr uint32_t idesc_g = idesc_bf16_f32(kBN, D, false, true);  // dV, dK: 128 x D
+        const uint32_t slot_addr = smem_u32(slots);
+        const bool leader = elect_one();
+        bool ok = true;
         for (int i = 0; ok && i < n_q; ++i) {
             const uint32_t b = i & 1;
             const int q_slot = (2 * i) % NSLOT, d_slot = (2 * i + 1) % NSLOT;
             const uint64_t qmn_desc = sdesc_sw128(slot_addr + q_slot * L::kTileBytes, kBQ * 128, 1024);
             const uint64_t dmn_desc = sdesc_sw128(slot_addr + d_slot * L::kTileBytes, kBQ * 128, 1024);
-            // dV += P^T dO_i
             if (!(ok = warp_wait(&p_ready[b], (i >> 1) & 1, a.status, kSitePReady))) break;
             tc_fence_after();
             if (leader) {
@@ -220,11 +234,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < kBQ / 16; ++kk)
                     mma_ts(tmem + kColDV, tmem + 64 * b + (kk >> 1) * 32 + (kk & 1) * 8,
                            sdesc_add(dmn_desc, kk * 2048), idesc_g, (i > 0 || kk > 0));
-                mma_commit(&slot_empty[d_slot]);
                 mma_commit(dv_done);
             }
             __syncwarp();
-            // dK += dS^T Q_i
             if (!(ok = warp_wait(&ds_ready[b], (i >> 1) & 1, a.status, kSiteDsReady))) break;
             tc_fence_after();
             if (leader) {
@@ -232,19 +244,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < kBQ / 16; ++kk)
                     mma_ts(tmem + kColDK, tmem + 128 + 64 * b + (kk >> 1) * 32 + (kk & 1) * 8,
                            sdesc_add(qmn_desc, kk * 2048), idesc_g, (i > 0 || kk > 0));
-                mma_commit(&slot_empty[q_slot]);
                 mma_commit(dk_done);
+                // S^T_i and dP^T_i (issuer A) completed before the compute warps produced dS^T_i, so after
+                // dK_i nothing reads Q_i or dO_i any more.
+                mma_commit(&slot_empty[q_slot]);
+                mma_commit(&slot_empty[d_slot]);
             }
             __syncwarp();
-            if (i + 2 < n_q) ok = issue_sdp(i + 2);
         }
         if (leader) mma_commit(final_bar);
         __syncwarp();
         warp_wait(final_bar, 0, a.status, kSiteFinal);
     } else {
         const int quarter = warp & 3;
-        const int g = (warp - 2) >> 2;           // column (query) half of every tile
-        const int tid = (warp - 2) * 32 + lane;  // 0..255; 0..127 load the stats
+        const int g = (warp - kFirstComputeWarp) >> 2;           // column (query) half of every tile
+        const int tid = (warp - kFirstComputeWarp) * 32 + lane;  // 0..255; 0..127 load the stats
         const int r = quarter * 32 + lane;       // key row within the tile (TMEM lane)
         const int key = k_tile * kBN + r;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;

@@ -12,7 +12,9 @@
 //   query rows here as there).
 //
 // GB300 mapping: warp 0 TMA producer (Q and dO once; 64-row K_j, V_j tiles
-// through a ring), warp 1 TMEM allocator + tcgen05 issuer, warps 2-9 compute:
+// through a ring); two tcgen05 issuer warps, warp 1 (also the TMEM allocator)
+// for S and dP and warp 2 for dQ, so that one keeps the tensor core fed while
+// the other waits on a barrier; warps 3-10 compute:
 // two warpgroups, each thread owning one query row (its TMEM lane) and one
 // half (32 keys) of every tile's columns -- dS is elementwise given the row's
 // L and D, so the halves never exchange data, and two warps per SM
@@ -26,9 +28,10 @@
 // MN-major form (keys are the reduction).  tcgen05.mma operations on different
 // accumulators are not ordered with each other, so every buffer is rewritten
 // only after its previous reader is known complete: the compute warps write
-// dS_j after S_j / dP_j completed, and the commit behind those tracks
-// dQ_{j-3}, the previous reader of dS[j % 3] (S_j is issued after dQ_{j-3}
-// and before dQ_{j-2}, hence three dS buffers).
+// dS_j after waiting for dQ_{j-3}, the previous reader of dS[j % 3] (three
+// buffers, so that wait is normally already satisfied); S_{j+2} / dP_{j+2}
+// overwrite S[b] / dP[b] only after the compute warps finished tile j.  K_j is
+// released after dQ_j, which is issued only after S_j completed.
 #include "fa_internal.h"
 #include "sm100_ptx.cuh"
 #include <cmath>
@@ -39,9 +42,11 @@ namespace {
 constexpr int kBM = 128;          // queries per CTA (TMEM lanes)
 constexpr int kBN = kDqKRows;     // keys per tile
 constexpr int kComputeWG = 2;     // compute warpgroups, one column half each
-constexpr int kThreads = 64 + 128 * kComputeWG;
+constexpr int kFirstComputeWarp = 3;
+constexpr int kThreads = 32 * kFirstComputeWarp + 128 * kComputeWG;
 
-enum : int { kSiteQ = 21, kSiteSlotEmpty, kSiteSlotFull, kSiteSFull, kSiteDsFull, kSiteDq, kSiteFinal, kSiteDrain };
+enum : int { kSiteQ = 21, kSiteSlotEmpty, kSiteSlotFull, kSiteSFull, kSiteDsFull, kSiteDq, kSiteFinal, kSiteDrain,
+             kSiteDqDone };
 
 template <int D, int NSLOT>
 struct DqSmem {
@@ -51,8 +56,8 @@ struct DqSmem {
     static constexpr int kDoOff = kQBytes;
     static constexpr int kSlotOff = 2 * kQBytes;
     static constexpr int kBarOff = kSlotOff + NSLOT * kTileBytes;
-    // q_full, slot_full[NSLOT], slot_empty[NSLOT], s_full[2], ds_full[2], final
-    static constexpr int kNumBars = 1 + 2 * NSLOT + 5;
+    // q_full, slot_full[NSLOT], slot_empty[NSLOT], s_full[2], ds_full[2], final, a_final, dq_done[3]
+    static constexpr int kNumBars = 1 + 2 * NSLOT + 9;
     static constexpr int kTmemHolderOff = kBarOff + kNumBars * 8;
     static constexpr int kAlloc = kTmemHolderOff + 16 + 1024;
 };
@@ -79,7 +84,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *slot_empty = slot_full + NSLOT;
     uint64_t *s_full = slot_empty + NSLOT;  // [2]: S_j and dP_j complete
     uint64_t *ds_full = s_full + 2;         // [2]: dS_j written (and S_j, dP_j read)
-    uint64_t *final_bar = ds_full + 2;
+    uint64_t *final_bar = ds_full + 2;  // issuer B: every dQ MMA has completed
+    uint64_t *a_final = final_bar + 1;  // issuer A: every S / dP MMA has completed
+    uint64_t *dq_done = a_final + 1;    // [3]: dQ_j completed (its dS buffer j % 3 is free)
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kTmemHolderOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -100,6 +107,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&ds_full[b], 128 * kComputeWG);
         }
         mbar_init(final_bar, 1);
+        mbar_init(a_final, 1);
+        for (int b = 0; b < 3; ++b) mbar_init(&dq_done[b], 1);
         fence_mbarrier_init();
     }
     if (warp == 1) {
@@ -146,23 +155,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        // MMA issuer: the whole warp runs the loop, one elected lane issues MMAs and their commits.
+        // Issuer A: S_j = Q K_j^T and dP_j = dO V_j^T into buffer j % 2.  The whole warp runs the loop
+        // (operands stay warp-uniform); one elected lane issues the MMAs and their commits.
         constexpr uint32_t idesc_sq = idesc_bf16_f32(kBM, kBN, false, false);  // S, dP: 128 x 64
-        constexpr uint32_t idesc_dq = idesc_bf16_f32(kBM, D, false, true);     // dQ += dS K: 128 x D
         const uint64_t q_desc = sdesc_sw128(smem_u32(q_s), 16, 1024);
         const uint64_t do_desc = sdesc_sw128(smem_u32(do_s), 16, 1024);
         const uint32_t slot_addr = smem_u32(slots);
         const bool leader = elect_one();
         bool ok = warp_wait(q_full, 0, a.status, kSiteQ);
         tc_fence_after();
-        // S_j = Q K_j^T and dP_j = dO V_j^T into buffer j % 2.  The compute warps have read
-        // S_{j-2} and dP_{j-2} (ds_full of tile j-2 was waited on before this is called).
-        auto issue_sdp = [&](int j) -> bool {
+        for (int j = 0; ok && j < n_kv; ++j) {
             const int k_slot = (2 * j) % NSLOT, k_round = (2 * j) / NSLOT;
             const int v_slot = (2 * j + 1) % NSLOT, v_round = (2 * j + 1) / NSLOT;
             const uint32_t b = j & 1;
-            if (!warp_wait(&slot_full[k_slot], k_round & 1, a.status, kSiteSlotFull)) return false;
-            if (!warp_wait(&slot_full[v_slot], v_round & 1, a.status, kSiteSlotFull)) return false;
+            // S[b], dP[b] last held tile j-2, which the compute warps have finished with
+            if (j >= 2 && !(ok = warp_wait(&ds_full[b], ((j - 2) >> 1) & 1, a.status, kSiteDsFull))) break;
+            if (!(ok = warp_wait(&slot_full[k_slot], k_round & 1, a.status, kSiteSlotFull))) break;
+            if (!(ok = warp_wait(&slot_full[v_slot], v_round & 1, a.status, kSiteSlotFull))) break;
             tc_fence_after();
             const uint64_t k_desc = sdesc_sw128(slot_addr + k_slot * L::kTileBytes, 16, 1024);
             const uint64_t v_desc = sdesc_sw128(slot_addr + v_slot * L::kTileBytes, 16, 1024);
@@ -179,24 +188,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(&slot_empty[v_slot]);  // V_j is no longer needed
             }
             __syncwarp();
-            return true;
-        };
-        if (ok) ok = issue_sdp(0);
-        if (ok && n_kv > 1) ok = issue_sdp(1);
+        }
+        // Drain this warp's MMAs before TMEM can be released (immediate in the normal path).
+        if (leader) mma_commit(a_final);
+        __syncwarp();
+        warp_wait(a_final, 0, a.status, kSiteFinal);
+    } else if (warp == 2) {
+        // Issuer B: dQ += dS_j K_j.
+        constexpr uint32_t idesc_dq = idesc_bf16_f32(kBM, D, false, true);  // dQ += dS K: 128 x D
+        const uint32_t slot_addr = smem_u32(slots);
+        const bool leader = elect_one();
+        bool ok = true;
         for (int j = 0; ok && j < n_kv; ++j) {
             const uint32_t b = j & 1;
             const int k_slot = (2 * j) % NSLOT;
             const uint64_t kmn_desc = sdesc_sw128(slot_addr + k_slot * L::kTileBytes, kBN * 128, 1024);
             if (!(ok = warp_wait(&ds_full[b], (j >> 1) & 1, a.status, kSiteDsFull))) break;
             tc_fence_after();
-            // S[b], dP[b] are free again: queue tile j+2 first so the compute warps never wait on dQ_j.
-            if (j + 2 < n_kv && !(ok = issue_sdp(j + 2))) break;
             if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)
                     mma_ts(tmem + kColDQ, tmem + kColDS + 32 * (j % 3) + kk * 8, sdesc_add(kmn_desc, kk * 2048),
                            idesc_dq, (j > 0 || kk > 0));
-                mma_commit(&slot_empty[k_slot]);
+                mma_commit(&dq_done[j % 3]);
+                mma_commit(&slot_empty[k_slot]);  // S_j completed before dS_j was produced
             }
             __syncwarp();
         }
@@ -205,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         warp_wait(final_bar, 0, a.status, kSiteFinal);
     } else {
         const int quarter = warp & 3;
-        const int g = (warp - 2) >> 2;  // column half of every tile
+        const int g = (warp - kFirstComputeWarp) >> 2;  // column half of every tile
         const int r = quarter * 32 + lane;
         const int row = q_tile * kBM + r;
         const bool valid = row < N;
@@ -245,6 +260,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const int key0 = j * kBN + g * kHalf;
             const bool need_mask = (key0 + kHalf > N) || (a.causal && key0 + kHalf - 1 > q_tile * kBM);
+            // dS[j % 3] was last read by dQ_{j-3}
+            if (j >= 3) {
+                ok = mbar_wait(&dq_done[j % 3], ((j / 3) - 1) & 1, a.status, kSiteDqDone);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tc_fence_after();
+            }
             uint32_t sraw[kHalf], praw[kHalf], dsk[kHalf / 2];
             tmem_ld32(tmem + lane_base + 64 * b + g * kHalf, sraw);
             tmem_ld32(tmem + lane_base + 128 + 64 * b + g * kHalf, praw);

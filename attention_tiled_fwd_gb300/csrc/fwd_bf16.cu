@@ -12,11 +12,13 @@
 //
 // GB300 mapping (one CTA = one 128-row query tile of one (batch, head)):
 //   warp 0      TMA producer: Q once, then K_j, V_j into an NSLOT-deep ring
-//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer:
-//                 S_j = Q K_j^T  (SS: both operands in shared memory) into one
-//                 of two S buffers in TMEM, then O += P_j V_j (TS: P_j, bf16, in
-//                 one of two P buffers in TMEM)
-//   warps 2-9   softmax, two warpgroups: a thread owns one query row (its TMEM
+//   warp 1      TMEM allocator + tcgen05 issuer A: S_j = Q K_j^T (SS: both
+//               operands in shared memory) into one of two S buffers in TMEM
+//   warp 2      tcgen05 issuer B: O += P_j V_j (TS: P_j, bf16, in one of two P
+//               buffers in TMEM).  Two issuers, because an MMA's issue blocks
+//               until the tensor core accepts it, so a single issuer leaves the
+//               tensor core idle whenever it waits on a barrier.
+//   warps 3-10  softmax, two warpgroups: a thread owns one query row (its TMEM
 //               lane) and one half of every S tile's columns.  The row max is
 //               thread-local within a half; the two halves of a row combine
 //               their maxima through shared memory (one bounded mbarrier
@@ -32,10 +34,11 @@
 //   product is one N = 256 MMA per 16-key step (D-blocking lives in the
 //   64-column panels of V and Q).
 //   Ordering: tcgen05.mma operations are only ordered among MMAs on the same
-//   accumulator, so no MMA ever writes TMEM columns an earlier MMA on another
-//   accumulator may still read.  P_j goes to P[j % 2]; the softmax writes it
-//   only after S_j completed, and the commit behind S_j tracks every earlier
-//   MMA, including PV_{j-2}, the last reader of P[j % 2].
+//   accumulator, and a commit tracks only its own thread's MMAs, so every TMEM
+//   buffer is rewritten only after its previous reader is known complete: the
+//   softmax writes P_j into P[j % 2] after waiting for PV_{j-2} (per-buffer
+//   barrier pv_done[j % 2]), and issuer A writes S_{j+2} into S[j % 2] after the
+//   softmax finished reading S_j.
 #include "fa_internal.h"
 #include "sm100_ptx.cuh"
 #include <cmath>
@@ -45,7 +48,8 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kSoftmaxWG = 2;  // softmax warpgroups, one column half each
-constexpr int kThreads = 64 + 128 * kSoftmaxWG;
+constexpr int kFirstSoftmaxWarp = 3;
+constexpr int kThreads = 32 * kFirstSoftmaxWarp + 128 * kSoftmaxWG;
 
 // Wait-site ids recorded in the status word on a time-out.
 enum : int { kSiteQ = 1, kSiteSlotEmpty, kSiteSlotFull, kSiteSFull, kSitePFull, kSitePV, kSiteFinal, kSiteDrain,
@@ -60,8 +64,9 @@ struct FwdSmem {
     static constexpr int kSlotOff = kQBytes;
     static constexpr int kXchgOff = kSlotOff + NSLOT * kSlotBytes;  // row-max exchange [2][2][128] + l [2][128]
     static constexpr int kBarOff = kXchgOff + (4 * kBM + 2 * kBM) * 4;
-    // barriers: q_full, slot_full[NSLOT], slot_empty[NSLOT], s_full[2], p_full[2], pv_done, final, xchg[2], lx
-    static constexpr int kNumBars = 1 + 2 * NSLOT + 2 + 2 + 1 + 1 + 3;
+    // barriers: q_full, slot_full[NSLOT], slot_empty[NSLOT], s_full[2], p_full[2], pv_done[2], final, a_final,
+    // xchg[2], lx
+    static constexpr int kNumBars = 1 + 2 * NSLOT + 2 + 2 + 2 + 1 + 1 + 3;
     static constexpr int kTmemHolderOff = kBarOff + kNumBars * 8;
     static constexpr int kBytes = kTmemHolderOff + 16;
     static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment of the base
@@ -87,9 +92,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *slot_empty = slot_full + NSLOT;
     uint64_t *s_full = slot_empty + NSLOT;
     uint64_t *p_full = s_full + 2;
-    uint64_t *pv_done = p_full + 2;
-    uint64_t *final_bar = pv_done + 1;
-    uint64_t *xchg = final_bar + 1;  // [2]: every softmax thread published its half-row max of a tile
+    uint64_t *pv_done = p_full + 2;     // [2]: PV_j completed (P buffer j % 2 is free again)
+    uint64_t *final_bar = pv_done + 2;  // issuer B: every PV MMA has completed (O is final)
+    uint64_t *a_final = final_bar + 1;  // issuer A: every S MMA has completed
+    uint64_t *xchg = a_final + 1;       // [2]: every softmax thread published its half-row max of a tile
     uint64_t *lx = xchg + 2;         // every softmax thread published its partial row sum
     float *smax = reinterpret_cast<float *>(smem + L::kXchgOff);  // [tile parity][half][row]
     float *lsum = smax + 4 * kBM;                                  // [half][row]
@@ -112,9 +118,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&s_full[b], 1);
             mbar_init(&p_full[b], 128 * kSoftmaxWG);
             mbar_init(&xchg[b], 128 * kSoftmaxWG);
+            mbar_init(&pv_done[b], 1);
         }
-        mbar_init(pv_done, 1);
         mbar_init(final_bar, 1);
+        mbar_init(a_final, 1);
         mbar_init(lx, 128 * kSoftmaxWG);
         fence_mbarrier_init();
     }
@@ -161,19 +168,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------------ MMA issuer A: S_j = Q K_j^T
         // The whole warp runs the loop (operands stay warp-uniform); one elected lane issues the MMAs
         // and the commits that track them.
         constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, BN, false, false);
-        constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, false, true);
         const uint64_t q_desc = sdesc_sw128(smem_u32(q_s), 16, 1024);
         const uint32_t slot_addr = smem_u32(slots);
         const bool leader = elect_one();
         bool ok = warp_wait(q_full, 0, a.status, kSiteQ);
         tc_fence_after();
-        auto issue_s = [&](int j) -> bool {
+        for (int j = 0; ok && j < n_kv; ++j) {
             const int idx = 2 * j, slot = idx % NSLOT, round = idx / NSLOT;
-            if (!warp_wait(&slot_full[slot], round & 1, a.status, kSiteSlotFull)) return false;
+            // S[j % 2] last held S_{j-2}; the softmax has read it once P_{j-2} is published
+            if (j >= 2 && !(ok = warp_wait(&p_full[j & 1], ((j - 2) >> 1) & 1, a.status, kSitePFull))) break;
+            if (!(ok = warp_wait(&slot_full[slot], round & 1, a.status, kSiteSlotFull))) break;
             tc_fence_after();
             const uint64_t k_desc = sdesc_sw128(slot_addr + slot * L::kSlotBytes, 16, 1024);
             const uint32_t d_s = tmem + ((j & 1) ? kColS1 : kColS0);
@@ -188,13 +196,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(&slot_empty[slot]);
             }
             __syncwarp();
-            return true;
-        };
-        if (ok) ok = issue_s(0);
-        if (ok && n_kv > 1) ok = issue_s(1);
+        }
+        // Drain this warp's MMAs before TMEM can be released (immediate in the normal path).
+        if (leader) mma_commit(a_final);
+        __syncwarp();
+        warp_wait(a_final, 0, a.status, kSiteFinal);
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ MMA issuer B: O += P_j V_j
+        constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, false, true);
+        const uint32_t slot_addr = smem_u32(slots);
+        const bool leader = elect_one();
+        bool ok = true;
         for (int j = 0; ok && j < n_kv; ++j) {
             if (!(ok = warp_wait(&p_full[j & 1], (j >> 1) & 1, a.status, kSitePFull))) break;
-            tc_fence_after();
             const int idx = 2 * j + 1, slot = idx % NSLOT, round = idx / NSLOT;
             if (!(ok = warp_wait(&slot_full[slot], round & 1, a.status, kSiteSlotFull))) break;
             tc_fence_after();
@@ -205,12 +219,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < BN / 16; ++kk)
                     mma_ts(tmem + kColO, p_t + kk * 8, sdesc_add(v_desc, kk * 2048), idesc_o, (j > 0 || kk > 0));
                 mma_commit(&slot_empty[slot]);
-                mma_commit(pv_done);
+                mma_commit(&pv_done[j & 1]);
             }
             __syncwarp();
-            if (j + 2 < n_kv) ok = issue_s(j + 2);
         }
-        // Every MMA issued above has completed before TMEM is released.
+        // Every PV MMA has completed before O is read or TMEM released.
         if (leader) mma_commit(final_bar);
         __syncwarp();
         warp_wait(final_bar, 0, a.status, kSiteFinal);
@@ -218,8 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ softmax / correction / epilogue
         constexpr int HB = BN / kSoftmaxWG;  // S columns per thread per tile
         constexpr int HD = D / kSoftmaxWG;   // O columns per thread
-        const int quarter = warp & 3;        // TMEM lanes [32*quarter, 32*quarter + 32)
-        const int g = (warp - 2) >> 2;       // column half
+        const int quarter = warp & 3;                 // TMEM lanes [32*quarter, 32*quarter + 32)
+        const int g = (warp - kFirstSoftmaxWarp) >> 2;  // column half
         const int r = quarter * 32 + lane;
         const int row = q_tile * kBM + r;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
@@ -267,6 +280,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float m_base = (m_use == -INFINITY) ? 0.f : m_use;
             const float alpha = need ? ex2_approx(m - m_base) : 1.f;
             float rs = 0.f;
+            // P[j % 2] was last read by PV_{j-2}
+            if (j >= 2) {
+                ok = mbar_wait(&pv_done[j & 1], ((j >> 1) - 1) & 1, a.status, kSitePV);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tc_fence_after();
+            }
             // P = 2^(S - m) as bf16 pairs into this tile's P buffer (this half's columns).
             constexpr int kPk = HB >= 64 ? 32 : HB / 2;  // packed pairs per store (32 or 16 columns)
 #pragma unroll
@@ -288,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             m = m_use;
             if (j > 0 && __any_sync(0xffffffffu, need)) {
                 // O must hold P_{j-1} V_{j-1} before it is rescaled (this half's columns).
-                ok = mbar_wait(pv_done, (j - 1) & 1, a.status, kSitePV);
+                ok = mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, a.status, kSitePV);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc_fence_after();
                 uint32_t ov[32];
@@ -307,9 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&p_full[j & 1]);
         }
         if (ok) {
-            // O is final once every MMA has completed: final_bar has a single phase, committed by the
-            // issuer after its last MMA.  (Waiting on pv_done's parity here would be ambiguous: only
-            // PV_{n-3} is known to be complete at this point, so pv_done may be two phases behind.)
+            // O is final once every PV MMA has completed: final_bar has a single phase, committed by
+            // issuer B after its last MMA.
             ok = mbar_wait(final_bar, 0, a.status, kSiteFinal);
             ok = __all_sync(0xffffffffu, ok);
         }
