@@ -19,7 +19,7 @@ FA_ERR_SCALE, FA_ERR_CUDA, FA_ERR_TIMEOUT, FA_ERR_DEVICE_PTR, FA_ERR_DEVICE = -6
 
 # Every symbol include/fa.h declares.
 EXPORTS = ("fa_forward", "fa_backward_dq", "fa_backward_dkdv", "fa_status_string", "fa_device_status",
-           "fa_selftest_timeout", "fa_version")
+           "fa_selftest_timeout", "fa_selftest_exp2", "fa_version")
 
 _lib = None
 
@@ -43,9 +43,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_device_status.argtypes = [_p]
     lib.fa_selftest_timeout.argtypes = [_i, _p]
+    lib.fa_selftest_exp2.argtypes = [_p, _p, _i, _p]
     lib.fa_version.argtypes = []
     for name in ("fa_forward", "fa_backward_dq", "fa_backward_dkdv", "fa_device_status",
-                 "fa_selftest_timeout", "fa_version"):
+                 "fa_selftest_timeout", "fa_selftest_exp2", "fa_version"):
         getattr(lib, name).restype = _i
     _lib = lib
     return lib

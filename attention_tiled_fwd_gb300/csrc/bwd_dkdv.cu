@@ -117,9 +117,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(&s_full[b], 1);
             mbar_init(&dp_full[b], 1);
-            mbar_init(&p_ready[b], 128 * kComputeWG);
-            mbar_init(&ds_ready[b], 128 * kComputeWG);
-            mbar_init(&stats_bar[b], 128 * kComputeWG);
+            mbar_init(&p_ready[b], 4 * kComputeWG);  // one arrive per compute warp
+            mbar_init(&ds_ready[b], 4 * kComputeWG);
+            mbar_init(&stats_bar[b], 4 * kComputeWG);
         }
         mbar_init(dv_done, 1);
         mbar_init(dk_done, 1);
@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         bool ok = true;
         store_stat(0, load_stat(q_begin));
-        mbar_arrive(&stats_bar[0]);
+        warp_arrive(&stats_bar[0]);
         for (int i = 0; i < n_q; ++i) {
             const int qt = q_begin + i;
             const int b = i & 1;
@@ -332,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st16(tmem + lane_base + 64 * b + g * kHalf, pk);
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&p_ready[b]);
+            warp_arrive(&p_ready[b]);
 
             ok = mbar_wait(&dp_full[b], (i >> 1) & 1, a.status, kSiteDpFull);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -358,12 +358,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&ds_ready[b]);
+            warp_arrive(&ds_ready[b]);
             // Publish the next tile's stats into the other buffer.  Its readers (tile i-1) are done:
             // every compute thread arrived on this tile's stats barrier only after finishing tile i-1.
             if (i + 1 < n_q) {
                 store_stat(b ^ 1, nxt);
-                mbar_arrive(&stats_bar[b ^ 1]);
+                warp_arrive(&stats_bar[b ^ 1]);
             }
         }
         if (ok) {

@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&s_full[b], 1);
-            mbar_init(&ds_full[b], 128 * kComputeWG);
+            mbar_init(&ds_full[b], 4 * kComputeWG);  // one arrive per compute warp
         }
         mbar_init(final_bar, 1);
         mbar_init(a_final, 1);
@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st16(tmem + lane_base + kColDS + 32 * (j % 3) + g * (kHalf / 2), dsk);
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&ds_full[b]);
+            warp_arrive(&ds_full[b]);
         }
         if (ok) {
             ok = mbar_wait(final_bar, 0, a.status, kSiteDq);  // single phase: every MMA has completed

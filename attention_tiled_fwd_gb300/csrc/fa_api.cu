@@ -271,4 +271,25 @@ extern "C" int fa_selftest_timeout(int limit_us, void *stream) {
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+namespace fa {
+namespace {
+__global__ void selftest_exp2_kernel(const float *x, float *y, int n) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) y[i] = ex2_fma(x[i]);
+}
+}  // namespace
+}  // namespace fa
+
+extern "C" int fa_selftest_exp2(const float *x, float *y, int n, void *stream) {
+    if (n < 1) return FA_ERR_SHAPE;
+    int rc = check_ptrs({x, y});
+    if (rc != FA_OK) return rc;
+    int dev;
+    DeviceState *st;
+    rc = device_state(&dev, &st);
+    if (rc != FA_OK) return rc;
+    selftest_exp2_kernel<<<(n + 255) / 256, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(x, y, n);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 extern "C" int fa_version(void) { return 100; }

@@ -116,13 +116,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&s_full[b], 1);
-            mbar_init(&p_full[b], 128 * kSoftmaxWG);
-            mbar_init(&xchg[b], 128 * kSoftmaxWG);
+            mbar_init(&p_full[b], 4 * kSoftmaxWG);  // one arrive per softmax warp
+            mbar_init(&xchg[b], 4 * kSoftmaxWG);
             mbar_init(&pv_done[b], 1);
         }
         mbar_init(final_bar, 1);
         mbar_init(a_final, 1);
-        mbar_init(lx, 128 * kSoftmaxWG);
+        mbar_init(lx, 4 * kSoftmaxWG);
         fence_mbarrier_init();
     }
     if (warp == 1) {
@@ -264,12 +264,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < HB; ++i)
                     if (key0 + i > lim) s[i] = -INFINITY;
             }
-            float mt = s[0];
+            // row max over this half: 8 independent partial maxima, then a small tree
+            float mx[8];
 #pragma unroll
-            for (int i = 1; i < HB; ++i) mt = fmaxf(mt, s[i]);
+            for (int u = 0; u < 8; ++u) mx[u] = s[u];
+#pragma unroll
+            for (int i = 8; i < HB; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
+            float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
             // combine with the other half of the row
             smax[((j & 1) * 2 + g) * kBM + r] = mt;
-            mbar_arrive(&xchg[j & 1]);
+            warp_arrive(&xchg[j & 1]);
             ok = mbar_wait(&xchg[j & 1], (j >> 1) & 1, a.status, kSiteXchg);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             mt = fmaxf(mt, smax[((j & 1) * 2 + (g ^ 1)) * kBM + r]);
@@ -279,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float m_use = need ? m_new : m;
             const float m_base = (m_use == -INFINITY) ? 0.f : m_use;
             const float alpha = need ? ex2_approx(m - m_base) : 1.f;
-            float rs = 0.f;
+            float rsum[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial row sums
             // P[j % 2] was last read by PV_{j-2}
             if (j >= 2) {
                 ok = mbar_wait(&pv_done[j & 1], ((j >> 1) - 1) & 1, a.status, kSitePV);
@@ -295,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < kPk; ++i) {
                     const float p0 = ex2_approx(s[ch * 64 + 2 * i] - m_base);
                     const float p1 = ex2_approx(s[ch * 64 + 2 * i + 1] - m_base);
-                    rs += p0 + p1;
+                    rsum[i & 3] += p0 + p1;
                     pk[i] = pack_bf16x2(p0, p1);
                 }
                 if constexpr (kPk == 32)
@@ -303,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else
                     tmem_st16(tmem + lane_base + p_col + ch * 32, pk);
             }
-            l = l * alpha + rs;
+            l = l * alpha + ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3]));
             m = m_use;
             if (j > 0 && __any_sync(0xffffffffu, need)) {
                 // O must hold P_{j-1} V_{j-1} before it is rescaled (this half's columns).
@@ -323,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&p_full[j & 1]);
+            warp_arrive(&p_full[j & 1]);
         }
         if (ok) {
             // O is final once every PV MMA has completed: final_bar has a single phase, committed by
@@ -333,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok) {
             lsum[g * kBM + r] = l;
-            mbar_arrive(lx);
+            warp_arrive(lx);
             ok = mbar_wait(lx, 0, a.status, kSiteXchg);
             ok = __all_sync(0xffffffffu, ok);
         }

@@ -82,6 +82,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *s
     }
 }
 
+// One arrive per warp: the warp's lanes synchronise (which orders their earlier
+// shared-memory writes and tcgen05 fences before the release), then lane 0
+// arrives.  Barriers the compute warps signal count warps, not threads: a
+// few hundred single-thread arrives on one barrier word serialise.
+__device__ __forceinline__ void warp_arrive(uint64_t *bar) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 // Whole-warp bounded wait: every lane waits, and the warp agrees on the outcome
 // (so warp-collective code after it stays convergent).
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int *status, int site) {
@@ -244,6 +253,25 @@ __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// 2^x on the FMA/ALU pipes, for offloading part of a softmax's exponentials
+// from the special-function unit.  Cody-Waite style split x = e + f with
+// e = floor(x) (adding 1.5 * 2^23 with round-down leaves floor(x) in the low
+// mantissa bits, so no conversion instruction is needed) and f in [0, 1);
+// 2^f from a degree-3 polynomial, minimax in relative error on [0, 1)
+// (Remez exchange fitted for this library: max relative error 7.5e-5, i.e.
+// 13.7 bits, ample for a bf16 P); 2^e applied by adding e to the exponent
+// field.  Arguments are clamped to >= -125 so the result stays a normal float
+// (2^-125 stands in for anything smaller).
+__device__ __forceinline__ float ex2_fma(float x) {
+    x = fmaxf(x, -125.f);
+    const float t = __fadd_rd(x, 12582912.f);  // 12582912 = 1.5 * 2^23
+    const float f = x - (t - 12582912.f);
+    float p = fmaf(f, 0.07802452f, 0.22606716f);
+    p = fmaf(p, f, 0.69583356f);
+    p = fmaf(p, f, 0.99992520f);
+    return __int_as_float(__float_as_int(p) + ((__float_as_int(t) - 0x4B400000) << 23));
 }
 
 // Two floats -> packed bf16x2 (round-to-nearest-even), lo in the low half.

@@ -127,6 +127,14 @@ FA_API int fa_device_status(void *stream);
  */
 FA_API int fa_selftest_timeout(int limit_us, void *stream);
 
+/*
+ * fa_selftest_exp2 -- test hook: y[i] = 2^x[i] computed on the FMA pipe the
+ * way the forward kernel computes a quarter of its softmax exponentials
+ * (range split + degree-3 polynomial, relative error < 1e-4 for x >= -125).
+ * x, y: n floats of device memory.  Returns FA_OK if launched.
+ */
+FA_API int fa_selftest_exp2(const float *x, float *y, int n, void *stream);
+
 /* Library version (major*10000 + minor*100 + patch). */
 FA_API int fa_version(void);
 
