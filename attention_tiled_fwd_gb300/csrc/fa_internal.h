@@ -7,17 +7,22 @@
 
 namespace fa {
 
-// Spec table for the tensor-core paths: query tile BM x key tile BN, K/V ring
-// depth, keyed by head dimension.  Picked so that S (double-buffered, BN
-// fp32 columns each) plus the D-column O accumulator fit the 512 TMEM
-// columns and the staged tiles fill (but do not exceed) shared memory.
+// Spec table of the bf16 forward: query rows per CTA, keys per K/V tile, K/V
+// ring depth, keyed by head dimension.  Picked so that the score, P and O
+// buffers fit the 512 TMEM columns and the staged tiles fill (but do not
+// exceed) shared memory.
+//   D = 64, 128: two 128-row query tiles per CTA (fwd_bf16_pair.cu); TMEM per
+//                tile S 64 + P 32 + O D columns; shared memory 2 Q tiles + ring.
+//   D = 256:     one 128-row query tile, two softmax warpgroups splitting the
+//                columns (fwd_bf16.cu); TMEM S 2x64 + P 2x32 + O 256 (one
+//                N = 256 accumulator, D-blocked shared-memory panels).
 struct FwdSpec {
     int D, BM, BN, nslot;
 };
 constexpr FwdSpec kFwdSpecs[] = {
-    {64, 128, 128, 8},   // Q 16 KB + 8 x 16 KB ring; TMEM 2x128 + 64
-    {128, 128, 128, 4},  // Q 32 KB + 4 x 32 KB ring; TMEM 2x128 + 128
-    {256, 128, 64, 4},   // Q 64 KB + 4 x 32 KB ring; TMEM 2x64 + 256 (D-blocked O)
+    {64, 256, 64, 12},  // Q 2 x 16 KB + 12 x 8 KB ring
+    {128, 256, 64, 8},  // Q 2 x 32 KB + 8 x 16 KB ring
+    {256, 128, 64, 4},  // Q 64 KB + 4 x 32 KB ring
 };
 
 // Tile rows of the backward kernels' streamed operands (TMA box heights).
@@ -55,6 +60,8 @@ struct TmaPair {
 cudaError_t launch_fwd_f32(const FwdArgs &a, cudaStream_t s);
 cudaError_t launch_fwd_bf16(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
                             const CUtensorMap &tv, cudaStream_t s);
+cudaError_t launch_fwd_bf16_pair(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
+                                 const CUtensorMap &tv, cudaStream_t s);
 cudaError_t launch_bwd_dq(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
                           const CUtensorMap &tv, const CUtensorMap &tdo, cudaStream_t s);
 cudaError_t launch_bwd_dkdv(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,

@@ -1,4 +1,6 @@
-// fwd_bf16.cu -- bf16 attention forward on the 5th-generation tensor cores
+// fwd_bf16.cu -- bf16 attention forward on the 5th-generation tensor cores,
+// one 128-row query tile per CTA; used for D = 256 (D = 64 and 128 run the
+// two-tile kernel of fwd_bf16_pair.cu, which does not fit D = 256 in TMEM)
 // (tcgen05, accumulators in TMEM), K/V tiles streamed by TMA through an
 // mbarrier ring in shared memory.
 //
@@ -394,8 +396,8 @@ cudaError_t launch_spec(const FwdArgs &a, const CUtensorMap &tq, const CUtensorM
 cudaError_t launch_fwd_bf16(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             cudaStream_t s) {
     switch (a.D) {
-        case 64: return launch_spec<64, 128, 8>(a, tq, tk, tv, s);
-        case 128: return launch_spec<128, 128, 4>(a, tq, tk, tv, s);
+        case 64:
+        case 128: return launch_fwd_bf16_pair(a, tq, tk, tv, s);  // two query tiles per CTA
         case 256: return launch_spec<256, 64, 4>(a, tq, tk, tv, s);
         default: return cudaErrorInvalidValue;
     }

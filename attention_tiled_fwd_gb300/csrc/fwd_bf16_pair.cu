@@ -1,0 +1,375 @@
+// fwd_bf16_pair.cu -- bf16 attention forward, D in {64, 128}: each CTA owns a
+// pair of 128-row query tiles of one (batch, head) and streams 64-key K/V tiles
+// past both.  Same algorithm as fwd_bf16.cu ("Learning Metal with
+// FlashAttention", section "FlashAttention"; metalworking "Flash Attention",
+// kernel anatomy items 1-5; metal-flash-attention forward pseudocode): Q tiles
+// resident, S = Q K^T in TMEM, online base-2 softmax with running max m and
+// sum l, O += P V in TMEM, O / l and L = m + ln(l) written once; causal tiles
+// above the diagonal are never loaded.
+//
+// GB300 mapping (why a pair): one softmax warpgroup owns each query tile, so a
+// thread owns a whole row (its TMEM lane) and the row max / sum are
+// thread-local -- no exchange between warps -- while the two warpgroups run
+// out of phase and hide each other's TMEM-load, barrier and SFU latencies.
+//   warp 0      TMA producer: Q_A, Q_B once, then K_j, V_j (64 rows) into a ring
+//   warp 1      TMEM allocator + tcgen05 issuer of S_X = Q_X K_j^T (X = A, B)
+//   warp 2      tcgen05 issuer of O_X += P_X V_j
+//   warps 3-6   softmax of tile A; warps 7-10 softmax of tile B
+// TMEM (per tile X): S_X (64 fp32 columns), P_X (32 columns of bf16 pairs),
+// O_X (D columns).  S_X is single-buffered but released early: the softmax
+// signals s_free as soon as S_X(j) is in registers, so S_X(j+1) runs on the
+// tensor core while the softmax exponentiates tile j.  The O correction is
+// lazy (only when the running max grows by more than 2^8).
+// Ordering: MMAs on different accumulators are not ordered with each other
+// and a commit tracks only its own thread's MMAs, so every reuse is explicit:
+// S_X(j+1) is issued after s_free(j); the softmax writes P_X(j) after
+// pv_done_X(j-1) (PV_X(j-1) read P_X and wrote O_X); O is read after the
+// single-phase final barrier.
+#include "fa_internal.h"
+#include "sm100_ptx.cuh"
+#include <cmath>
+
+namespace fa {
+namespace {
+
+constexpr int kBM = 128;            // rows per query tile (TMEM lanes)
+constexpr int kBN = 64;             // keys per K/V tile
+constexpr int kTiles = 2;           // query tiles per CTA
+constexpr int kFirstSoftmaxWarp = 3;
+constexpr int kThreads = 32 * kFirstSoftmaxWarp + 128 * kTiles;
+
+enum : int { kSiteQ = 61, kSiteSlotEmpty, kSiteSlotFull, kSiteSFull, kSiteSFree, kSitePFull, kSitePV, kSiteFinal,
+             kSiteDrain };
+
+template <int D, int NSLOT>
+struct PairSmem {
+    static constexpr int kPanels = D / 64;
+    static constexpr int kQBytes = kBM * D * 2;    // one query tile
+    static constexpr int kSlotBytes = kBN * D * 2;  // one K or V tile
+    static constexpr int kQOff = 0;
+    static constexpr int kSlotOff = kTiles * kQBytes;
+    static constexpr int kBarOff = kSlotOff + NSLOT * kSlotBytes;
+    // q_full, slot_full[NSLOT], slot_empty[NSLOT], per tile: s_full, s_free, p_full, pv_done; final, a_final
+    static constexpr int kNumBars = 1 + 2 * NSLOT + 4 * kTiles + 2;
+    static constexpr int kTmemHolderOff = kBarOff + kNumBars * 8;
+    static constexpr int kAlloc = kTmemHolderOff + 16 + 1024;
+};
+
+template <int D, int NSLOT>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                         const __grid_constant__ CUtensorMap tmap_v, FwdArgs a) {
+    using L = PairSmem<D, NSLOT>;
+    constexpr int kPanels = L::kPanels;
+    constexpr uint32_t kTmemCols = 512;
+    // TMEM columns: S_A, S_B, P_A, P_B, then O_A, O_B
+    constexpr uint32_t kColS = 0, kColP = 2 * kBN, kColO = 256;
+    static_assert(kColP + kTiles * (kBN / 2) <= kColO && kColO + kTiles * D <= kTmemCols, "TMEM budget");
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *q_s = smem + L::kQOff;
+    uint8_t *slots = smem + L::kSlotOff;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
+    uint64_t *q_full = bars;
+    uint64_t *slot_full = bars + 1;
+    uint64_t *slot_empty = slot_full + NSLOT;
+    uint64_t *s_full = slot_empty + NSLOT;  // [tile]: S_X(j) complete
+    uint64_t *s_free = s_full + kTiles;     // [tile]: softmax holds S_X(j) in registers
+    uint64_t *p_full = s_free + kTiles;     // [tile]: P_X(j) written (and O_X corrected)
+    uint64_t *pv_done = p_full + kTiles;    // [tile]: PV_X(j) complete
+    uint64_t *final_bar = pv_done + kTiles; // issuer B: every PV MMA has completed
+    uint64_t *a_final = final_bar + 1;      // issuer A: every S MMA has completed
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kTmemHolderOff);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int blk = gridDim.x - 1 - blockIdx.x;  // heaviest causal blocks first
+    const int bh = blockIdx.z * a.H + blockIdx.y;
+    const int N = a.N;
+    const int row0 = blk * (kTiles * kBM);
+    // K/V tiles query tile x needs (0 if the tile lies past N)
+    auto tiles_of = [&](int x) -> int {
+        const int r0 = row0 + x * kBM;
+        const int kv_end = a.causal ? min(N, r0 + kBM) : N;
+        return r0 < N ? (kv_end + kBN - 1) / kBN : 0;
+    };
+    const int n_kv0 = tiles_of(0), n_kv1 = tiles_of(1);
+    const int n_all = max(n_kv0, n_kv1);  // tiles streamed (>= 1)
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < NSLOT; ++s) {
+            mbar_init(&slot_full[s], 1);
+            mbar_init(&slot_empty[s], 1);
+        }
+        for (int x = 0; x < kTiles; ++x) {
+            mbar_init(&s_full[x], 1);
+            mbar_init(&s_free[x], 4);  // one arrive per softmax warp of tile x
+            mbar_init(&p_full[x], 4);
+            mbar_init(&pv_done[x], 1);
+        }
+        mbar_init(final_bar, 1);
+        mbar_init(a_final, 1);
+        fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmap_q);
+            tma_prefetch_desc(&tmap_k);
+            tma_prefetch_desc(&tmap_v);
+            // only query tiles that start below N are loaded (a tile wholly past N has no work)
+            const int n_q_tiles = (row0 + kBM < N) ? kTiles : 1;
+            mbar_arrive_expect_tx(q_full, n_q_tiles * L::kQBytes);
+            for (int x = 0; x < n_q_tiles; ++x)
+#pragma unroll
+                for (int p = 0; p < kPanels; ++p)
+                    tma_load_3d(q_s + x * L::kQBytes + p * (kBM * 128), &tmap_q, q_full, p * 64, row0 + x * kBM, bh);
+            int last_round[NSLOT];
+#pragma unroll
+            for (int s = 0; s < NSLOT; ++s) last_round[s] = -1;
+            for (int idx = 0; idx < 2 * n_all; ++idx) {
+                const int slot = idx % NSLOT, round = idx / NSLOT;
+                if (!mbar_wait(&slot_empty[slot], (round & 1) ^ 1, a.status, kSiteSlotEmpty)) break;
+                uint8_t *dst = slots + slot * L::kSlotBytes;
+                const CUtensorMap *map = (idx & 1) ? &tmap_v : &tmap_k;
+                mbar_arrive_expect_tx(&slot_full[slot], L::kSlotBytes);
+#pragma unroll
+                for (int p = 0; p < kPanels; ++p)
+                    tma_load_3d(dst + p * (kBN * 128), map, &slot_full[slot], p * 64, (idx >> 1) * kBN, bh);
+#pragma unroll
+                for (int s = 0; s < NSLOT; ++s)
+                    if (s == slot) last_round[s] = round;
+            }
+            // Drain: never leave the CTA with a TMA write still in flight.
+#pragma unroll
+            for (int s = 0; s < NSLOT; ++s)
+                if (last_round[s] >= 0) mbar_wait(&slot_full[s], last_round[s] & 1, a.status, kSiteDrain);
+            mbar_wait(q_full, 0, a.status, kSiteDrain);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ issuer A: S_X(j) = Q_X K_j^T
+        // The whole warp runs the loop (operands stay warp-uniform); one elected lane issues the MMAs
+        // and the commits that track them.
+        constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, false, false);
+        const uint64_t q_desc = sdesc_sw128(smem_u32(q_s), 16, 1024);
+        const uint32_t slot_addr = smem_u32(slots);
+        const bool leader = elect_one();
+        bool ok = warp_wait(q_full, 0, a.status, kSiteQ);
+        tc_fence_after();
+        for (int j = 0; ok && j < n_all; ++j) {
+            const int slot = (2 * j) % NSLOT, round = (2 * j) / NSLOT;
+            if (!(ok = warp_wait(&slot_full[slot], round & 1, a.status, kSiteSlotFull))) break;
+            tc_fence_after();
+            const uint64_t k_desc = sdesc_sw128(slot_addr + slot * L::kSlotBytes, 16, 1024);
+#pragma unroll
+            for (int x = 0; x < kTiles; ++x) {
+                if (j >= (x == 0 ? n_kv0 : n_kv1)) continue;
+                // S_X is single-buffered: the softmax must hold S_X(j-1) in registers
+                if (j >= 1 && !(ok = warp_wait(&s_free[x], (j - 1) & 1, a.status, kSiteSFree))) break;
+                tc_fence_after();
+                if (leader) {
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint32_t off = (ks >> 2) * (kBM * 128) + (ks & 3) * 32;
+                        mma_ss(tmem + kColS + x * kBN, sdesc_add(q_desc, x * L::kQBytes + off),
+                               sdesc_add(k_desc, (ks >> 2) * (kBN * 128) + (ks & 3) * 32), idesc_s, ks > 0);
+                    }
+                    mma_commit(&s_full[x]);
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (leader) mma_commit(&slot_empty[slot]);  // K_j read by both S MMAs
+            __syncwarp();
+        }
+        // Drain this warp's MMAs before TMEM can be released (immediate in the normal path).
+        if (leader) mma_commit(a_final);
+        __syncwarp();
+        warp_wait(a_final, 0, a.status, kSiteFinal);
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ issuer B: O_X += P_X(j) V_j
+        constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, false, true);
+        const uint32_t slot_addr = smem_u32(slots);
+        const bool leader = elect_one();
+        bool ok = true;
+        for (int j = 0; ok && j < n_all; ++j) {
+            const int slot = (2 * j + 1) % NSLOT, round = (2 * j + 1) / NSLOT;
+            if (!(ok = warp_wait(&slot_full[slot], round & 1, a.status, kSiteSlotFull))) break;
+            const uint64_t v_desc = sdesc_sw128(slot_addr + slot * L::kSlotBytes, kBN * 128, 1024);
+#pragma unroll
+            for (int x = 0; x < kTiles; ++x) {
+                if (j >= (x == 0 ? n_kv0 : n_kv1)) continue;
+                if (!(ok = warp_wait(&p_full[x], j & 1, a.status, kSitePFull))) break;
+                tc_fence_after();
+                if (leader) {
+#pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk)
+                        mma_ts(tmem + kColO + x * D, tmem + kColP + x * (kBN / 2) + kk * 8,
+                               sdesc_add(v_desc, kk * 2048), idesc_o, (j > 0 || kk > 0));
+                    mma_commit(&pv_done[x]);
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (leader) mma_commit(&slot_empty[slot]);  // V_j read by both PV MMAs
+            __syncwarp();
+        }
+        if (leader) mma_commit(final_bar);
+        __syncwarp();
+        warp_wait(final_bar, 0, a.status, kSiteFinal);
+    } else {
+        // ------------------------------------------------------------ softmax / correction / epilogue
+        const int x = (warp - kFirstSoftmaxWarp) >> 2;  // query tile of this warpgroup
+        const int quarter = warp & 3;                   // TMEM lanes [32*quarter, 32*quarter + 32)
+        const int r = quarter * 32 + lane;
+        const int tile_row0 = row0 + x * kBM;
+        const int row = tile_row0 + r;
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const uint32_t s_col = kColS + x * kBN, p_col = kColP + x * (kBN / 2), o_col = kColO + x * D;
+        const float c = a.scale_log2;
+        const int n = x == 0 ? n_kv0 : n_kv1;
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n; ++j) {
+            ok = mbar_wait(&s_full[x], j & 1, a.status, kSiteSFull);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            tc_fence_after();
+            float s[kBN];
+            {
+                uint32_t raw[kBN];
+                tmem_ld32(tmem + lane_base + s_col, raw);
+                tmem_ld32(tmem + lane_base + s_col + 32, raw + 32);
+                tmem_wait_ld();
+                tc_fence_before();
+                warp_arrive(&s_free[x]);  // S_X may be overwritten now
+#pragma unroll
+                for (int i = 0; i < kBN; ++i) s[i] = __uint_as_float(raw[i]) * c;
+            }
+            const int key0 = j * kBN;
+            const bool need_mask = (key0 + kBN > N) || (a.causal && key0 + kBN - 1 > tile_row0);
+            if (need_mask) {
+                const int lim = a.causal ? min(N - 1, row) : N - 1;  // last visible key
+#pragma unroll
+                for (int i = 0; i < kBN; ++i)
+                    if (key0 + i > lim) s[i] = -INFINITY;
+            }
+            float mx[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) mx[u] = s[u];
+#pragma unroll
+            for (int i = 8; i < kBN; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
+            const float mt =
+                fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+            const float m_new = fmaxf(m, mt);
+            // Lazy correction: keep the stale max unless the row max grew by > 8 (factor 256).
+            const bool need = m_new > m + 8.f;
+            const float m_use = need ? m_new : m;
+            const float m_base = (m_use == -INFINITY) ? 0.f : m_use;
+            const float alpha = need ? ex2_approx(m - m_base) : 1.f;
+            float rsum[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t pk[kBN / 2];
+#pragma unroll
+            for (int i = 0; i < kBN / 2; ++i) {
+                const float p0 = ex2_approx(s[2 * i] - m_base);
+                const float p1 = ex2_approx(s[2 * i + 1] - m_base);
+                rsum[i & 3] += p0 + p1;
+                pk[i] = pack_bf16x2(p0, p1);
+            }
+            l = l * alpha + ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3]));
+            m = m_use;
+            // P_X and O_X were last touched by PV_X(j-1)
+            if (j >= 1) {
+                ok = mbar_wait(&pv_done[x], (j - 1) & 1, a.status, kSitePV);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tc_fence_after();
+            }
+            tmem_st32(tmem + lane_base + p_col, pk);
+            if (j >= 1 && __any_sync(0xffffffffu, need)) {
+                uint32_t ov[32];
+#pragma unroll
+                for (int ch = 0; ch < D / 32; ++ch) {
+                    tmem_ld32(tmem + lane_base + o_col + ch * 32, ov);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                    tmem_st32(tmem + lane_base + o_col + ch * 32, ov);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            warp_arrive(&p_full[x]);
+        }
+        if (ok && n > 0) {
+            ok = mbar_wait(final_bar, 0, a.status, kSiteFinal);  // single phase: every PV has completed
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        if (ok && n > 0) {
+            tc_fence_after();
+            const float inv_l = 1.f / l;
+            __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.o) + ((size_t)bh * N + row) * D;
+            uint32_t ov[32];
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch) {
+                tmem_ld32(tmem + lane_base + o_col + ch * 32, ov);
+                tmem_wait_ld();
+                if (row < N) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + ch * 32);
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(ov[v4 * 8 + 0]) * inv_l, __uint_as_float(ov[v4 * 8 + 1]) * inv_l);
+                        w.y = pack_bf16x2(__uint_as_float(ov[v4 * 8 + 2]) * inv_l, __uint_as_float(ov[v4 * 8 + 3]) * inv_l);
+                        w.z = pack_bf16x2(__uint_as_float(ov[v4 * 8 + 4]) * inv_l, __uint_as_float(ov[v4 * 8 + 5]) * inv_l);
+                        w.w = pack_bf16x2(__uint_as_float(ov[v4 * 8 + 6]) * inv_l, __uint_as_float(ov[v4 * 8 + 7]) * inv_l);
+                        dst[v4] = w;
+                    }
+                }
+            }
+            if (row < N) a.lse[(size_t)bh * N + row] = (m + __log2f(l)) * 0.69314718055994531f;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int D, int NSLOT>
+cudaError_t launch_spec(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                        cudaStream_t s) {
+    using L = PairSmem<D, NSLOT>;
+    static_assert(L::kAlloc <= 232448, "shared memory budget");
+    auto kern = fwd_bf16_pair_kernel<D, NSLOT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    if (e != cudaSuccess) return e;
+    dim3 grid((a.N + kTiles * kBM - 1) / (kTiles * kBM), a.H, a.B);
+    kern<<<grid, kThreads, L::kAlloc, s>>>(tq, tk, tv, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_bf16_pair(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
+                                 const CUtensorMap &tv, cudaStream_t s) {
+    switch (a.D) {
+        case 64: return launch_spec<64, 12>(a, tq, tk, tv, s);
+        case 128: return launch_spec<128, 8>(a, tq, tk, tv, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace fa
