@@ -69,6 +69,9 @@ def _load():
             lib.fa_oracle_backward_dkdv_rows.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int64,
                                                          ctypes.c_int64, ctypes.c_double, ctypes.c_int,
                                                          ctypes.c_int64, _ip, _dp, _dp]
+            lib.fa_oracle_forward_kv.argtypes = [_dp, _dp, _dp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                                 ctypes.c_double, ctypes.c_int, _dp, _dp]
+            lib.fa_oracle_forward_kv.restype = ctypes.c_int
             for f in (lib.fa_oracle_forward_rows, lib.fa_oracle_backward_head,
                       lib.fa_oracle_backward_dq_rows, lib.fa_oracle_backward_dkdv_rows):
                 f.restype = ctypes.c_int
@@ -118,6 +121,25 @@ def forward(q, k, v, scale: float, causal: bool, threads: Optional[int] = None):
         _check(lib.fa_oracle_forward_rows(_ptr(q[b, h]), _ptr(k[b, h]), _ptr(v[b, h]), N, D,
                                           float(scale), int(bool(causal)), N, None,
                                           _ptr(o[b, h]), _ptr(lse[b, h])), "forward")
+
+    _map_heads(one, [(b, h) for b in range(B) for h in range(H)], threads)
+    return o, lse
+
+
+def forward_kv(q, k, v, scale: float, causal: bool, threads: Optional[int] = None):
+    """Decode form: q [B,H,n_q,D] against k, v [B,H,N_k,D]; the query rows are the last n_q
+    positions (causal: row i sees keys j <= N_k - n_q + i).  Returns O [B,H,n_q,D], LSE [B,H,n_q]."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, nq, D = q.shape
+    nk = k.shape[2]
+    o = np.empty((B, H, nq, D))
+    lse = np.empty((B, H, nq))
+    lib = _load()
+
+    def one(bh):
+        b, h = bh
+        _check(lib.fa_oracle_forward_kv(_ptr(q[b, h]), _ptr(k[b, h]), _ptr(v[b, h]), nq, nk, D, float(scale),
+                                        int(bool(causal)), _ptr(o[b, h]), _ptr(lse[b, h])), "forward_kv")
 
     _map_heads(one, [(b, h) for b in range(B) for h in range(H)], threads)
     return o, lse

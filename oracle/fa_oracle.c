@@ -289,3 +289,35 @@ int fa_oracle_backward_dkdv_rows(const double *q, const double *k, const double 
     }
     return 0;
 }
+
+/*
+ * Decode form: n_q query rows against N_k keys of one head (q is [n_q, D],
+ * k and v are [N_k, D]).  The query rows are the LAST n_q positions of the
+ * sequence, so with causal masking query row i sees keys j <= N_k - n_q + i
+ * (for n_q = N_k this is the self-attention rule above); without it every
+ * row sees all N_k keys.  Same plain definition: full score row, row-max
+ * shifted softmax, O_i = sum_j P_ij v_j, lse_i = m_i + ln(l_i).
+ *   o : [n_q, D],  lse : [n_q]
+ */
+int fa_oracle_forward_kv(const double *q, const double *k, const double *v,
+                         int64_t n_q, int64_t N_k, int64_t D, double scale, int causal,
+                         double *o, double *lse)
+{
+    if (n_q < 1 || N_k < 1 || D < 1 || n_q > N_k)
+        return -1;
+    double *p = (double *)malloc((size_t)N_k * sizeof(double));
+    if (!p)
+        return -1;
+    for (int64_t i = 0; i < n_q; ++i) {
+        int64_t nvis = causal ? N_k - n_q + i + 1 : N_k;
+        score_row(q + i * D, k, nvis, D, scale, p);
+        lse[i] = softmax_row(p, nvis);
+        for (int64_t d = 0; d < D; ++d)
+            o[i * D + d] = 0.0;
+        for (int64_t j = 0; j < nvis; ++j)
+            for (int64_t d = 0; d < D; ++d)
+                o[i * D + d] += p[j] * v[j * D + d];
+    }
+    free(p);
+    return 0;
+}

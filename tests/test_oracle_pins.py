@@ -272,6 +272,39 @@ def test_row_ranges_sum_to_full_backward(causal):
         np.testing.assert_allclose(hi[(b, h)]["o"], g["o"][b, h, 9:], atol=1e-13)
 
 
+# ---------------------------------------------------------------------------
+# Decode form (n_q query rows that are the last n_q positions, against N_k keys)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("causal", [False, True])
+def test_decode_form_equals_self_attention_rows(causal):
+    """The last n_q rows of self-attention over N_k positions are exactly the decode form."""
+    B, H, N, D, nq = 1, 2, 19, 8, 5
+    q, k, v = (_rand((B, H, N, D), 100 + s) for s in range(3))
+    o_full, l_full = oracle.forward(q, k, v, 0.45, causal)
+    o, l = oracle.forward_kv(q[:, :, N - nq:], k, v, 0.45, causal)
+    np.testing.assert_allclose(o, o_full[:, :, N - nq:], atol=1e-13)
+    np.testing.assert_allclose(l, l_full[:, :, N - nq:], atol=1e-13)
+
+
+def test_decode_form_closed_forms_and_library():
+    """Q = 0 gives the mean of the visible V rows (causal: the first N_k - n_q + i + 1);
+    general inputs match torch float64 SDPA with an explicit end-aligned causal mask."""
+    B, H, N, D, nq = 2, 1, 23, 6, 4
+    k, v = _rand((B, H, N, D), 110), _rand((B, H, N, D), 111)
+    o, lse = oracle.forward_kv(np.zeros((B, H, nq, D)), k, v, 0.3, True)
+    for i in range(nq):
+        nvis = N - nq + i + 1
+        np.testing.assert_allclose(o[:, :, i], v[:, :, :nvis].mean(axis=2), atol=1e-13)
+        np.testing.assert_allclose(lse[:, :, i], math.log(nvis), atol=1e-13)
+    q = _rand((B, H, nq, D), 112)
+    mask = torch.tensor(np.arange(N)[None, :] <= (N - nq + np.arange(nq))[:, None])
+    for causal in (False, True):
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.tensor(q), torch.tensor(k), torch.tensor(v), attn_mask=mask if causal else None, scale=0.3)
+        o, _ = oracle.forward_kv(q, k, v, 0.3, causal)
+        np.testing.assert_allclose(o, ref.numpy(), atol=1e-12)
+
+
 def test_rejects_bad_arguments():
     q = np.zeros((1, 1, 4, 2))
     with pytest.raises(RuntimeError):
