@@ -20,8 +20,8 @@ import torch
 from . import _native
 from ._native import FA_BF16, FA_F32, FAError
 
-__all__ = ["fa_forward", "fa_backward_dq", "fa_backward_dkdv", "fa_device_status", "fa_selftest_timeout",
-           "FAError", "FA_BF16", "FA_F32", "attention_flops"]
+__all__ = ["fa_forward", "fa_backward_dq", "fa_backward_dkdv", "fa_decode", "fa_decode_workspace_bytes",
+           "fa_device_status", "fa_selftest_timeout", "FAError", "FA_BF16", "FA_F32", "attention_flops"]
 
 _DT = {torch.bfloat16: FA_BF16, torch.float32: FA_F32}
 
@@ -109,6 +109,41 @@ def fa_backward_dkdv(q, k, v, dO, lse, delta, scale: Optional[float] = None, cau
                               _dtype_code(dk), _stream_ptr(stream))
     _native.check(rc, "fa_backward_dkdv")
     return dk, dv
+
+
+def fa_decode_workspace_bytes(B: int, H: int, n_q: int, N: int, D: int) -> int:
+    """Workspace bytes fa_decode needs (fa_decode_workspace_bytes)."""
+    import ctypes
+    out = ctypes.c_size_t(0)
+    _native.check(_native.load().fa_decode_workspace_bytes(B, H, n_q, N, D, ctypes.byref(out)),
+                  "fa_decode_workspace_bytes")
+    return int(out.value)
+
+
+def fa_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: Optional[float] = None,
+              causal: bool = False, o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+              workspace: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None):
+    """Decode: q [B, H, n_q, D] (the last n_q positions) against k, v [B, H, N, D] (fa_decode).
+
+    The workspace is a CUDA uint8 tensor of at least fa_decode_workspace_bytes(...) bytes; one is
+    allocated here when the caller passes none.  Returns (o, lse)."""
+    B, H, nq, D = _shape4(q, "q")
+    Bk, Hk, N, Dk = _shape4(k, "k")
+    if (Bk, Hk, Dk) != (B, H, D) or _shape4(v, "v") != (B, H, N, D):
+        raise ValueError("k and v must be [B, H, N, D] matching q's B, H, D")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, nq), dtype=torch.float32, device=q.device)
+    need = fa_decode_workspace_bytes(B, H, nq, N, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    lib = _native.load()
+    rc = lib.fa_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, nq, N, D, _scale(scale, D),
+                       int(bool(causal)), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                       _stream_ptr(stream))
+    _native.check(rc, "fa_decode")
+    return o, lse
 
 
 def fa_device_status(stream: Optional[torch.cuda.Stream] = None) -> int:

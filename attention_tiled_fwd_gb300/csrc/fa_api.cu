@@ -207,6 +207,44 @@ extern "C" int fa_backward_dkdv(const void *q, const void *k, const void *v, con
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+namespace {
+int check_decode(int B, int H, int n_q, int N, int D, float scale) {
+    int rc = check_shape(B, H, N, D, scale);
+    if (rc != FA_OK) return rc;
+    if (D != 64 && D != 128 && D != 256) return FA_ERR_HEAD_DIM;
+    if (n_q < 1 || n_q > decode_max_rows(D) || n_q > N) return FA_ERR_SHAPE;
+    if ((long long)B * H * (long long)n_q > (1ll << 31) - 1) return FA_ERR_SHAPE;
+    return FA_OK;
+}
+}  // namespace
+
+extern "C" int fa_decode_workspace_bytes(int B, int H, int n_q, int N, int D, size_t *bytes) {
+    if (!bytes) return FA_ERR_NULL;
+    int rc = check_decode(B, H, n_q, N, D, 1.f);
+    if (rc != FA_OK) return rc;
+    *bytes = decode_workspace_bytes(B, H, n_q, N, D);
+    return FA_OK;
+}
+
+extern "C" int fa_decode(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int n_q,
+                         int N, int D, float scale, int causal, void *workspace, size_t workspace_bytes,
+                         void *stream) {
+    int rc = check_decode(B, H, n_q, N, D, scale);
+    if (rc != FA_OK) return rc;
+    rc = check_ptrs({q, k, v, o, lse, workspace});
+    if (rc != FA_OK) return rc;
+    if (workspace_bytes < decode_workspace_bytes(B, H, n_q, N, D)) return FA_ERR_WORKSPACE;
+    int dev;
+    DeviceState *st;
+    rc = device_state(&dev, &st);
+    if (rc != FA_OK) return rc;
+    DecodeArgs a{q, k, v, o, lse, static_cast<float *>(workspace), B, H, n_q, N, D, 0, 0, scale * log2e(),
+                 causal ? 1 : 0};
+    decode_split(B, H, N, D, &a.splits, &a.chunk);
+    cudaError_t e = launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 extern "C" const char *fa_status_string(int status) {
     switch (status) {
         case FA_OK: return "ok";
@@ -220,6 +258,7 @@ extern "C" const char *fa_status_string(int status) {
         case FA_ERR_TIMEOUT: return "a bounded in-kernel wait ran out";
         case FA_ERR_DEVICE_PTR: return "pointer is not device-accessible memory";
         case FA_ERR_DEVICE: return "current device is not sm_103 (GB300)";
+        case FA_ERR_WORKSPACE: return "workspace smaller than fa_decode_workspace_bytes() requires";
         default: return "unknown status";
     }
 }

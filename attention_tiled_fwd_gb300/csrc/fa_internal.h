@@ -52,6 +52,25 @@ struct BwdArgs {
     int *status;
 };
 
+// Decode (few query rows against a long key range), split over the keys.
+constexpr int kDecodeTargetCtas = 4 * 152;  // aim: several CTAs per SM across all (batch, head) pairs
+
+struct DecodeArgs {
+    const void *q, *k, *v;  // q [B, H, n_q, D]; k, v [B, H, N, D]; bf16
+    void *o;                // [B, H, n_q, D] bf16
+    float *lse;             // [B, H, n_q]
+    float *workspace;       // O, m, l partials of every key chunk (decode_workspace_bytes)
+    int B, H, n_q, N, D;
+    int splits, chunk;      // key chunks per (batch, head), keys per chunk
+    float scale_log2;
+    int causal;
+};
+
+int decode_max_rows(int D);
+void decode_split(int B, int H, int N, int D, int *splits, int *chunk);
+size_t decode_workspace_bytes(int B, int H, int n_q, int N, int D);
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
+
 // Tensor maps for one [B*H, N, D] bf16 tensor, box = {64, rows, 1}, 128-byte swizzle.
 struct TmaPair {
     CUtensorMap map;

@@ -246,6 +246,63 @@ def run_reference(args, w, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------- decode (one GPU, own line)
+DECODE_SHAPE = dict(B=4, H=32, n_q=1, N=32768, D=128)  # one new token against a 32K-entry K/V cache
+
+
+def decode_main(args):
+    """Decode throughput: GB/s of algorithmic traffic (K and V read once, q read, O and LSE written)
+    against the measured HBM copy bandwidth; L2 flushed before every timed call."""
+    import torch
+    import attention_tiled_fwd_gb300 as fa
+    dev = torch.device("cuda", 0)
+    B, H, nq, N, D = (DECODE_SHAPE[k] for k in ("B", "H", "n_q", "N", "D"))
+    g = torch.Generator().manual_seed(2024)
+    q = torch.randn(B, H, nq, D, generator=g).bfloat16().to(dev)
+    k = torch.randn(B, H, N, D, generator=g).bfloat16().to(dev)
+    v = torch.randn(B, H, N, D, generator=g).bfloat16().to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, nq, device=dev)
+    ws = torch.empty(fa.fa_decode_workspace_bytes(B, H, nq, N, D), dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        fa.fa_decode(q, k, v, causal=True, o=o, lse=lse, workspace=ws, stream=stream)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(0)
+    sampler.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    sampler.mark_start()
+    for e0, e1 in evs:
+        flush.fill_(0.0)
+        e0.record(stream)
+        fa.fa_decode(q, k, v, causal=True, o=o, lse=lse, workspace=ws, stream=stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark_stop()
+    clocks = sampler.stop()
+    if fa.fa_device_status() != 0:
+        raise RuntimeError("device status reports a failure")
+    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+    algo_bytes = 2 * B * H * N * D * 2 + B * H * nq * D * 2 * 2 + B * H * nq * 4
+    gbs = algo_bytes / (ms * 1e-3) / 1e9
+    peaks, kind = load_peaks()
+    peak = float(peaks["hbm_gbs"])
+    line = {"metric": "decode attention GB/s (K/V cache read once; bf16)", "value": gbs, "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1))",
+            "config": {"workload": "decode", **DECODE_SHAPE, "causal": True,
+                       "l2": "flushed before every timed call (512 MB write), outside the timed events"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                         "traffic": None, "peak_source": f"{kind} hbm_gbs (copy)"},
+            "gpu_launches": 2 * args.steps, "clocks": clocks}
+    print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------------------------- GPU arm
 def main():
     ap = argparse.ArgumentParser()
@@ -259,6 +316,10 @@ def main():
     ap.add_argument("--grad-dtype", choices=("bf16", "f32"), default="bf16")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+
+    if args.workload == "decode":
+        decode_main(args)
+        return
 
     from synthetic_inputs import WORKLOADS, make_qkv
     w = WORKLOADS[args.workload]

@@ -38,6 +38,8 @@
 #ifndef FA_H_
 #define FA_H_
 
+#include <stddef.h>
+
 #if defined(__GNUC__)
 #define FA_API __attribute__((visibility("default")))
 #else
@@ -65,7 +67,8 @@ enum fa_status {
     FA_ERR_CUDA = -7,        /* the CUDA runtime reported an error (launch, attributes)  */
     FA_ERR_TIMEOUT = -8,     /* a bounded in-kernel wait ran out (read by fa_device_status) */
     FA_ERR_DEVICE_PTR = -9,  /* a pointer is not device-accessible memory                */
-    FA_ERR_DEVICE = -10      /* the current device is not sm_100-family (tcgen05)        */
+    FA_ERR_DEVICE = -10,     /* the current device is not sm_103 (GB300)                 */
+    FA_ERR_WORKSPACE = -11   /* a workspace is smaller than its size query requires      */
 };
 
 /*
@@ -107,6 +110,31 @@ FA_API int fa_backward_dkdv(const void *q, const void *k, const void *v, const v
                      const float *lse, const float *delta, void *dk, void *dv,
                      int B, int H, int N, int D, float scale, int causal, int dtype,
                      int grad_dtype, void *stream);
+
+/*
+ * fa_decode -- attention of a few query rows against a long key/value range
+ * (decode).  "Flash Attention" (metalworking), section on the technique's
+ * boundaries: one query row cannot fill a matrix-engine tile, so decode gets a
+ * separate vector kernel; the mathematics is the forward's:
+ *   O = softmax(scale q K^T) V per query row, LSE = natural log-sum-exp.
+ *   q: [B, H, n_q, D]; k, v: [B, H, N, D]; o: [B, H, n_q, D]; all bf16.
+ *   lse: [B, H, n_q] fp32.  1 <= n_q <= N; n_q <= 16 (n_q <= 8 when D = 256);
+ *   D in {64, 128, 256}.  The query rows are the LAST n_q positions: with
+ *   causal != 0, row i sees keys j <= N - n_q + i; otherwise all N keys.
+ *   workspace: device memory owned by the caller, at least
+ *   fa_decode_workspace_bytes(...) bytes, 16-byte aligned; it holds the
+ *   partial results of the key chunks the work is split into (no clearing
+ *   needed; its contents are undefined afterwards).  Two calls that run
+ *   concurrently must not share a workspace.
+ * Errors as for fa_forward, plus FA_ERR_WORKSPACE when workspace_bytes is too
+ * small.  Launches two kernels on `stream`.
+ */
+FA_API int fa_decode(const void *q, const void *k, const void *v, void *o, float *lse,
+                     int B, int H, int n_q, int N, int D, float scale, int causal,
+                     void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of workspace fa_decode needs for these sizes (written to *bytes). */
+FA_API int fa_decode_workspace_bytes(int B, int H, int n_q, int N, int D, size_t *bytes);
 
 /* Static description of a status code (never NULL). */
 FA_API const char *fa_status_string(int status);
