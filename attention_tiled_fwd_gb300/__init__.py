@@ -21,6 +21,7 @@ from . import _native
 from ._native import FA_BF16, FA_F32, FAError
 
 __all__ = ["fa_forward", "fa_backward_dq", "fa_backward_dkdv", "fa_decode", "fa_decode_workspace_bytes",
+           "fa_decode_noalloc",
            "fa_device_status", "fa_selftest_timeout", "FAError", "FA_BF16", "FA_F32", "attention_flops"]
 
 _DT = {torch.bfloat16: FA_BF16, torch.float32: FA_F32}
@@ -143,6 +144,26 @@ def fa_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: Optional
                        int(bool(causal)), _ptr(workspace), workspace.numel() * workspace.element_size(),
                        _stream_ptr(stream))
     _native.check(rc, "fa_decode")
+    return o, lse
+
+
+def fa_decode_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
+                      scale: Optional[float] = None, causal: bool = False,
+                      stream: Optional[torch.cuda.Stream] = None):
+    """fa_decode with no workspace (fa_decode_noalloc): the partials go to the library's fixed
+    per-device scratch, so the call allocates nothing; the caller passes the outputs o
+    [B, H, n_q, D] bf16 and lse [B, H, n_q] fp32.  Calls that overlap in time on one device race on
+    that scratch; sizes needing more than FA_DECODE_NOALLOC_SCRATCH_BYTES raise FAError
+    (FA_ERR_SCRATCH_LIMIT).  Returns (o, lse)."""
+    B, H, nq, D = _shape4(q, "q")
+    Bk, Hk, N, Dk = _shape4(k, "k")
+    if (Bk, Hk, Dk) != (B, H, D) or _shape4(v, "v") != (B, H, N, D):
+        raise ValueError("k and v must be [B, H, N, D] matching q's B, H, D")
+    if _shape4(o, "o") != (B, H, nq, D) or tuple(lse.shape) != (B, H, nq):
+        raise ValueError("o must be [B, H, n_q, D] and lse [B, H, n_q]")
+    rc = _native.load().fa_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, nq, N, D,
+                                          _scale(scale, D), int(bool(causal)), _stream_ptr(stream))
+    _native.check(rc, "fa_decode_noalloc")
     return o, lse
 
 

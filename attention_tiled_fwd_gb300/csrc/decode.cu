@@ -25,8 +25,15 @@
 #include "fa_internal.h"
 #include "sm100_ptx.cuh"
 #include <cmath>
+#include <mutex>
 
 namespace fa {
+
+// Scratch for fa_decode_noalloc: the same partials as the caller's workspace
+// of fa_decode, held in the library's own static device storage (one copy per
+// device, reserved when the module loads) so that the entry point allocates
+// nothing.  Sizes that need more are rejected before launch.
+static __device__ __align__(256) float g_decode_scratch[kDecodeScratchBytes / sizeof(float)];
 
 namespace {
 
@@ -296,6 +303,29 @@ size_t decode_workspace_bytes(int B, int H, int n_q, int N, int D) {
     int splits, chunk;
     decode_split(B, H, N, D, &splits, &chunk);
     return sizeof(float) * (size_t)B * H * splits * n_q * (size_t)(D + 2);
+}
+
+namespace {
+constexpr int kScratchDevices = 64;
+float *g_scratch_addr[kScratchDevices];
+std::mutex g_scratch_mu;
+}  // namespace
+
+cudaError_t decode_static_scratch(float **ptr) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kScratchDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        // once per device, with that device current; a failure is returned and retried on the next call
+        void *addr = nullptr;
+        e = cudaGetSymbolAddress(&addr, g_decode_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_addr[dev] = static_cast<float *>(addr);
+    }
+    *ptr = g_scratch_addr[dev];
+    return cudaSuccess;
 }
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s) {

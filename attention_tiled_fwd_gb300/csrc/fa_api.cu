@@ -245,6 +245,29 @@ extern "C" int fa_decode(const void *q, const void *k, const void *v, void *o, f
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+static_assert(kDecodeScratchBytes == FA_DECODE_NOALLOC_SCRATCH_BYTES, "scratch size differs from fa.h");
+
+// fa_decode with the partials in the library's static scratch instead of a
+// caller workspace: same validation and kernels, no allocation anywhere.
+extern "C" int fa_decode_noalloc(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                                 int n_q, int N, int D, float scale, int causal, void *stream) {
+    int rc = check_decode(B, H, n_q, N, D, scale);
+    if (rc != FA_OK) return rc;
+    if (decode_workspace_bytes(B, H, n_q, N, D) > kDecodeScratchBytes) return FA_ERR_SCRATCH_LIMIT;
+    rc = check_ptrs({q, k, v, o, lse});
+    if (rc != FA_OK) return rc;
+    int dev;
+    DeviceState *st;
+    rc = device_state(&dev, &st);
+    if (rc != FA_OK) return rc;
+    float *scratch = nullptr;
+    if (decode_static_scratch(&scratch) != cudaSuccess) return FA_ERR_CUDA;
+    DecodeArgs a{q, k, v, o, lse, scratch, B, H, n_q, N, D, 0, 0, scale * log2e(), causal ? 1 : 0};
+    decode_split(B, H, N, D, &a.splits, &a.chunk);
+    cudaError_t e = launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 extern "C" const char *fa_status_string(int status) {
     switch (status) {
         case FA_OK: return "ok";
@@ -259,6 +282,8 @@ extern "C" const char *fa_status_string(int status) {
         case FA_ERR_DEVICE_PTR: return "pointer is not device-accessible memory";
         case FA_ERR_DEVICE: return "current device is not sm_103 (GB300)";
         case FA_ERR_WORKSPACE: return "workspace smaller than fa_decode_workspace_bytes() requires";
+        case FA_ERR_SCRATCH_LIMIT:
+            return "sizes need more than FA_DECODE_NOALLOC_SCRATCH_BYTES of scratch; use fa_decode with a workspace";
         default: return "unknown status";
     }
 }

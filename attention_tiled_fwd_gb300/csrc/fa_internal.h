@@ -71,6 +71,12 @@ void decode_split(int B, int H, int N, int D, int *splits, int *chunk);
 size_t decode_workspace_bytes(int B, int H, int n_q, int N, int D);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
 
+// Fixed scratch of fa_decode_noalloc (static device storage in decode.cu).
+constexpr size_t kDecodeScratchBytes = size_t(16) << 20;
+// Device address of the current device's scratch; the first call on a device
+// looks it up (cudaGetSymbolAddress), later calls return the cached address.
+cudaError_t decode_static_scratch(float **ptr);
+
 // Tensor maps for one [B*H, N, D] bf16 tensor, box = {64, rows, 1}, 128-byte swizzle.
 struct TmaPair {
     CUtensorMap map;

@@ -68,7 +68,8 @@ enum fa_status {
     FA_ERR_TIMEOUT = -8,     /* a bounded in-kernel wait ran out (read by fa_device_status) */
     FA_ERR_DEVICE_PTR = -9,  /* a pointer is not device-accessible memory                */
     FA_ERR_DEVICE = -10,     /* the current device is not sm_103 (GB300)                 */
-    FA_ERR_WORKSPACE = -11   /* a workspace is smaller than its size query requires      */
+    FA_ERR_WORKSPACE = -11,  /* a workspace is smaller than its size query requires      */
+    FA_ERR_SCRATCH_LIMIT = -12 /* the sizes need more than FA_DECODE_NOALLOC_SCRATCH_BYTES */
 };
 
 /*
@@ -135,6 +136,40 @@ FA_API int fa_decode(const void *q, const void *k, const void *v, void *o, float
 
 /* Bytes of workspace fa_decode needs for these sizes (written to *bytes). */
 FA_API int fa_decode_workspace_bytes(int B, int H, int n_q, int N, int D, size_t *bytes);
+
+/* Size of the fixed per-device scratch that fa_decode_noalloc works in. */
+#define FA_DECODE_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/*
+ * fa_decode_noalloc -- fa_decode without a workspace argument.  The attention
+ * pages have no counterpart of this entry point: it is a library convenience.
+ *
+ * Who it is for: callers that cannot allocate device memory, or cannot keep a
+ * workspace alive, at the point where they decode -- a plain C host with no
+ * device allocator of its own, or a latency-critical loop where a cudaMalloc
+ * (which may synchronise the device) or an allocation that fails under a fully
+ * committed memory budget is not acceptable.  This call allocates nothing:
+ * the key-chunk partials go to a fixed scratch array that the library holds in
+ * static device storage, FA_DECODE_NOALLOC_SCRATCH_BYTES per device.
+ *
+ * Arguments, layout, results and errors are those of fa_decode, minus the
+ * workspace; in addition:
+ *   - sizes whose fa_decode_workspace_bytes() exceeds
+ *     FA_DECODE_NOALLOC_SCRATCH_BYTES are rejected with FA_ERR_SCRATCH_LIMIT
+ *     before anything is launched (use fa_decode with your own workspace);
+ *   - nothing in the scratch needs to start at zero: every entry a call reads
+ *     is written by that same call first;
+ *   - the first call on each device sets up that device's scratch address
+ *     (one cudaGetSymbolAddress with the device current); make that first
+ *     call before beginning any stream capture on the device;
+ *   - all calls on one device share the one scratch array, so calls that can
+ *     overlap in time (different streams without ordering between them, or
+ *     different host threads) race on it and give undefined results.  Calls
+ *     enqueued on one stream run one after another and are safe.
+ */
+FA_API int fa_decode_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
+                             int B, int H, int n_q, int N, int D, float scale, int causal,
+                             void *stream);
 
 /* Static description of a status code (never NULL). */
 FA_API const char *fa_status_string(int status);
