@@ -240,7 +240,7 @@ extern "C" int fa_decode(const void *q, const void *k, const void *v, void *o, f
     if (rc != FA_OK) return rc;
     DecodeArgs a{q, k, v, o, lse, static_cast<float *>(workspace), B, H, n_q, N, D, 0, 0, scale * log2e(),
                  causal ? 1 : 0};
-    decode_split(B, H, N, D, &a.splits, &a.chunk);
+    decode_split(B, H, n_q, N, D, &a.splits, &a.chunk);
     cudaError_t e = launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -263,7 +263,7 @@ extern "C" int fa_decode_noalloc(const void *q, const void *k, const void *v, vo
     float *scratch = nullptr;
     if (decode_static_scratch(&scratch) != cudaSuccess) return FA_ERR_CUDA;
     DecodeArgs a{q, k, v, o, lse, scratch, B, H, n_q, N, D, 0, 0, scale * log2e(), causal ? 1 : 0};
-    decode_split(B, H, N, D, &a.splits, &a.chunk);
+    decode_split(B, H, n_q, N, D, &a.splits, &a.chunk);
     cudaError_t e = launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

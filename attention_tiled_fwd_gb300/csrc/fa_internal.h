@@ -53,7 +53,8 @@ struct BwdArgs {
 };
 
 // Decode (few query rows against a long key range), split over the keys.
-constexpr int kDecodeTargetCtas = 4 * 152;  // aim: several CTAs per SM across all (batch, head) pairs
+constexpr int kNumSms = 152;                      // GB300
+constexpr int kDecodeTargetCtas = 4 * kNumSms;  // staged decode kernel: several CTAs per SM across all (batch, head) pairs
 
 struct DecodeArgs {
     const void *q, *k, *v;  // q [B, H, n_q, D]; k, v [B, H, N, D]; bf16
@@ -67,7 +68,7 @@ struct DecodeArgs {
 };
 
 int decode_max_rows(int D);
-void decode_split(int B, int H, int N, int D, int *splits, int *chunk);
+void decode_split(int B, int H, int n_q, int N, int D, int *splits, int *chunk);
 size_t decode_workspace_bytes(int B, int H, int n_q, int N, int D);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
 

@@ -59,8 +59,13 @@ def test_decode_rejects_before_launch(lib):
 
 
 # ------------------------------------------------------------------ GPU parity
-SHAPES = [(1, 1, 1, 1, 64), (2, 3, 1, 1000, 128), (1, 2, 4, 4133, 128), (1, 1, 16, 777, 64),
-          (1, 2, 8, 2000, 256), (2, 2, 16, 16, 128), (1, 1, 3, 129, 256), (1, 2, 2, 70000, 64)]
+# every (n_q <= 4, D) pair of the streaming kernel, the staged kernel's n_q 5..16, ragged chunk ends,
+# n_q = N, and one long single-head cache that is cut into many chunks
+SHAPES = [(1, 1, 1, 1, 64), (2, 3, 1, 1000, 128), (1, 3, 1, 5000, 256), (1, 2, 2, 70000, 64),
+          (2, 1, 2, 3333, 128), (1, 1, 2, 300, 256), (1, 2, 3, 999, 64), (1, 1, 3, 2500, 128),
+          (1, 1, 3, 129, 256), (1, 1, 4, 1500, 64), (1, 2, 4, 4133, 128), (2, 1, 4, 640, 256),
+          (1, 1, 4, 4, 128), (1, 1, 16, 777, 64), (1, 2, 8, 2000, 256), (2, 2, 16, 16, 128),
+          (1, 1, 5, 300, 128), (1, 1, 1, 200003, 128)]
 
 
 @pytest.mark.gpu
