@@ -53,8 +53,7 @@ struct BwdArgs {
 };
 
 // Decode (few query rows against a long key range), split over the keys.
-constexpr int kNumSms = 152;                      // GB300
-constexpr int kDecodeTargetCtas = 4 * kNumSms;  // staged decode kernel: several CTAs per SM across all (batch, head) pairs
+constexpr int kNumSms = 152;  // GB300
 
 struct DecodeArgs {
     const void *q, *k, *v;  // q [B, H, n_q, D]; k, v [B, H, N, D]; bf16

@@ -119,7 +119,7 @@ FA_API int fa_backward_dkdv(const void *q, const void *k, const void *v, const v
  * separate vector kernel; the mathematics is the forward's:
  *   O = softmax(scale q K^T) V per query row, LSE = natural log-sum-exp.
  *   q: [B, H, n_q, D]; k, v: [B, H, N, D]; o: [B, H, n_q, D]; all bf16.
- *   lse: [B, H, n_q] fp32.  1 <= n_q <= N; n_q <= 16 (n_q <= 8 when D = 256);
+ *   lse: [B, H, n_q] fp32.  1 <= n_q <= N; n_q <= 16;
  *   D in {64, 128, 256}.  The query rows are the LAST n_q positions: with
  *   causal != 0, row i sees keys j <= N - n_q + i; otherwise all N keys.
  *   workspace: device memory owned by the caller, at least

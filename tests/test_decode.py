@@ -34,7 +34,7 @@ def test_workspace_size_query(lib):
     # O, m, l partials: 4 bytes x B x H x chunks x n_q x (D + 2), at least one chunk
     assert out.value >= 4 * 2 * 3 * 4 * 130 and out.value % (4 * 2 * 3 * 4 * 130) == 0
     assert lib.fa_decode_workspace_bytes(1, 1, 17, 100, 128, ctypes.byref(out)) == nat.FA_ERR_SHAPE
-    assert lib.fa_decode_workspace_bytes(1, 1, 9, 100, 256, ctypes.byref(out)) == nat.FA_ERR_SHAPE
+    assert lib.fa_decode_workspace_bytes(1, 1, 17, 100, 256, ctypes.byref(out)) == nat.FA_ERR_SHAPE
     assert lib.fa_decode_workspace_bytes(1, 1, 5, 4, 64, ctypes.byref(out)) == nat.FA_ERR_SHAPE  # n_q > N
     assert lib.fa_decode_workspace_bytes(1, 1, 1, 100, 96, ctypes.byref(out)) == nat.FA_ERR_HEAD_DIM
     assert lib.fa_decode_workspace_bytes(1, 1, 1, 100, 64, None) == nat.FA_ERR_NULL
@@ -59,13 +59,13 @@ def test_decode_rejects_before_launch(lib):
 
 
 # ------------------------------------------------------------------ GPU parity
-# every (n_q <= 4, D) pair of the streaming kernel, the staged kernel's n_q 5..16, ragged chunk ends,
+# every (n_q <= 4, D) pair, n_q 5..16 in blocks of 4 rows (ragged last block), ragged chunk ends,
 # n_q = N, and one long single-head cache that is cut into many chunks
 SHAPES = [(1, 1, 1, 1, 64), (2, 3, 1, 1000, 128), (1, 3, 1, 5000, 256), (1, 2, 2, 70000, 64),
           (2, 1, 2, 3333, 128), (1, 1, 2, 300, 256), (1, 2, 3, 999, 64), (1, 1, 3, 2500, 128),
           (1, 1, 3, 129, 256), (1, 1, 4, 1500, 64), (1, 2, 4, 4133, 128), (2, 1, 4, 640, 256),
           (1, 1, 4, 4, 128), (1, 1, 16, 777, 64), (1, 2, 8, 2000, 256), (2, 2, 16, 16, 128),
-          (1, 1, 5, 300, 128), (1, 1, 1, 200003, 128)]
+          (1, 1, 5, 300, 128), (1, 1, 13, 1000, 256), (1, 2, 9, 8191, 128), (1, 1, 1, 200003, 128)]
 
 
 @pytest.mark.gpu
