@@ -101,8 +101,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kTmemHolderOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int k_tile = blockIdx.x;  // causal: tile 0 has the most query tiles, launched first
-    const int bh = blockIdx.z * a.H + blockIdx.y;
+    int rank, bh;
+    tile_order((a.N + kBN - 1) / kBN, a.B * a.H, a.causal, &rank, &bh);
+    const int k_tile = rank;  // causal: key tile 0 has the most query tiles
     const int N = a.N;
     const int n_q_total = (N + kBQ - 1) / kBQ;
     const int q_begin = a.causal ? (k_tile * kBN) / kBQ : 0;
@@ -422,7 +423,7 @@ cudaError_t launch_spec(const BwdArgs &a, const CUtensorMap &tq, const CUtensorM
     auto kern = bwd_dkdv_kernel<D, NSLOT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
-    dim3 grid((a.N + kBN - 1) / kBN, a.H, a.B);
+    dim3 grid(((a.N + kBN - 1) / kBN) * a.H * a.B);
     kern<<<grid, kThreads, L::kAlloc, s>>>(tq, tk, tv, tdo, a);
     return cudaGetLastError();
 }

@@ -90,8 +90,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kTmemHolderOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int q_tile = gridDim.x - 1 - blockIdx.x;  // heaviest causal tiles first
-    const int bh = blockIdx.z * a.H + blockIdx.y;
+    int rank, bh;
+    tile_order((a.N + kBM - 1) / kBM, a.B * a.H, a.causal, &rank, &bh);
+    const int q_tile = (a.N + kBM - 1) / kBM - 1 - rank;  // causal: the last query tile has the most keys
     const int N = a.N;
     const int kv_end = a.causal ? min(N, (q_tile + 1) * kBM) : N;
     const int n_kv = (kv_end + kBN - 1) / kBN;  // >= 1
@@ -341,7 +342,7 @@ cudaError_t launch_spec(const BwdArgs &a, const CUtensorMap &tq, const CUtensorM
     auto kern = bwd_dq_kernel<D, NSLOT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
-    dim3 grid((a.N + kBM - 1) / kBM, a.H, a.B);
+    dim3 grid(((a.N + kBM - 1) / kBM) * a.H * a.B);
     kern<<<grid, kThreads, L::kAlloc, s>>>(tq, tk, tv, tdo, a);
     return cudaGetLastError();
 }

@@ -12,7 +12,8 @@ namespace fa {
 // buffers fit the 512 TMEM columns and the staged tiles fill (but do not
 // exceed) shared memory.
 //   D = 64, 128: two 128-row query tiles per CTA (fwd_bf16_pair.cu); TMEM per
-//                tile S 64 + P 32 + O D columns; shared memory 2 Q tiles + ring.
+//                tile S 128 (P over its first 64) + O D columns; shared memory
+//                2 Q tiles + ring.
 //   D = 256:     one 128-row query tile, two softmax warpgroups splitting the
 //                columns (fwd_bf16.cu); TMEM S 2x64 + P 2x32 + O 256 (one
 //                N = 256 accumulator, D-blocked shared-memory panels).
@@ -20,14 +21,32 @@ struct FwdSpec {
     int D, BM, BN, nslot;
 };
 constexpr FwdSpec kFwdSpecs[] = {
-    {64, 256, 64, 12},  // Q 2 x 16 KB + 12 x 8 KB ring
-    {128, 256, 64, 8},  // Q 2 x 32 KB + 8 x 16 KB ring
+    {64, 256, 128, 10},  // Q 2 x 16 KB + 10 x 16 KB ring
+    {128, 256, 128, 5},  // Q 2 x 32 KB + 5 x 32 KB ring
     {256, 128, 64, 4},  // Q 64 KB + 4 x 32 KB ring
 };
 
 // Tile rows of the backward kernels' streamed operands (TMA box heights).
 constexpr int kDqKRows = 64;    // dQ kernel: 128 query rows per CTA, 64-key K/V tiles
 constexpr int kDkdvQRows = 64;  // dK/dV kernel: 128 keys per CTA, 64-query Q/dO tiles
+
+// Work order of a 1-D grid over (tile, batch*head).  Causal launches go by
+// tile rank across all heads, rank 0 (the most K/V tiles) first, so that the
+// hardware, which dispatches CTAs in index order, starts every SM on the
+// longest tiles and fills the tail with short ones.  Non-causal tiles are
+// equal, so the tiles of one head stay adjacent (they share its K/V in L2).
+#ifdef __CUDACC__
+__device__ __forceinline__ void tile_order(int n_tiles, int n_bh, bool causal, int *rank, int *bh) {
+    const int L = blockIdx.x;
+    if (causal) {
+        *rank = L / n_bh;
+        *bh = L % n_bh;
+    } else {
+        *rank = L % n_tiles;
+        *bh = L / n_tiles;
+    }
+}
+#endif
 
 struct FwdArgs {
     const void *q, *k, *v;

@@ -1,6 +1,6 @@
 // fwd_bf16_pair.cu -- bf16 attention forward, D in {64, 128}: each CTA owns a
-// pair of 128-row query tiles of one (batch, head) and streams 64-key K/V tiles
-// past both.  Same algorithm as fwd_bf16.cu ("Learning Metal with
+// pair of 128-row query tiles of one (batch, head) and streams 128-key K/V
+// tiles past both.  Same algorithm as fwd_bf16.cu ("Learning Metal with
 // FlashAttention", section "FlashAttention"; metalworking "Flash Attention",
 // kernel anatomy items 1-5; metal-flash-attention forward pseudocode): Q tiles
 // resident, S = Q K^T in TMEM, online base-2 softmax with running max m and
@@ -10,21 +10,24 @@
 // GB300 mapping (why a pair): one softmax warpgroup owns each query tile, so a
 // thread owns a whole row (its TMEM lane) and the row max / sum are
 // thread-local -- no exchange between warps -- while the two warpgroups run
-// out of phase and hide each other's TMEM-load, barrier and SFU latencies.
-//   warp 0      TMA producer: Q_A, Q_B once, then K_j, V_j (64 rows) into a ring
+// out of phase: the tensor core works on one tile's S or PV while the other
+// tile's softmax runs.
+//   warp 0      TMA producer: Q_A, Q_B once, then K_j, V_j (128 rows) into a ring
 //   warp 1      TMEM allocator + tcgen05 issuer of S_X = Q_X K_j^T (X = A, B)
 //   warp 2      tcgen05 issuer of O_X += P_X V_j
 //   warps 3-6   softmax of tile A; warps 7-10 softmax of tile B
-// TMEM (per tile X): S_X (64 fp32 columns), P_X (32 columns of bf16 pairs),
-// O_X (D columns).  S_X is single-buffered but released early: the softmax
-// signals s_free as soon as S_X(j) is in registers, so S_X(j+1) runs on the
-// tensor core while the softmax exponentiates tile j.  The O correction is
-// lazy (only when the running max grows by more than 2^8).
+// TMEM (512 columns): S_A, S_B (128 fp32 columns each), O_A, O_B (D columns
+// each).  128-key tiles keep the S MMA at N = 128, where it runs at the full
+// tensor rate (at N = 64 it is shared-memory-bound).  P_X(j) is written as
+// bf16 pairs over the first 64 columns of S_X(j), which the softmax has
+// already read, so S_X(j+1) is issued only after PV_X(j) has completed
+// (pv_done).  The O correction is lazy (only when the running max grows by
+// more than 2^8).
 // Ordering: MMAs on different accumulators are not ordered with each other
 // and a commit tracks only its own thread's MMAs, so every reuse is explicit:
-// S_X(j+1) is issued after s_free(j); the softmax writes P_X(j) after
-// pv_done_X(j-1) (PV_X(j-1) read P_X and wrote O_X); O is read after the
-// single-phase final barrier.
+// S_X(j+1) is issued after pv_done_X(j), which also orders the softmax's O
+// rescale of step j+1 after PV_X(j); O is read after the single-phase final
+// barrier.
 #include "fa_internal.h"
 #include "sm100_ptx.cuh"
 #include <cmath>
@@ -33,13 +36,12 @@ namespace fa {
 namespace {
 
 constexpr int kBM = 128;            // rows per query tile (TMEM lanes)
-constexpr int kBN = 64;             // keys per K/V tile
+constexpr int kBN = 128;            // keys per K/V tile
 constexpr int kTiles = 2;           // query tiles per CTA
 constexpr int kFirstSoftmaxWarp = 3;
 constexpr int kThreads = 32 * kFirstSoftmaxWarp + 128 * kTiles;
 
-enum : int { kSiteQ = 61, kSiteSlotEmpty, kSiteSlotFull, kSiteSFull, kSiteSFree, kSitePFull, kSitePV, kSiteFinal,
-             kSiteDrain };
+enum : int { kSiteQ = 61, kSiteSlotEmpty, kSiteSlotFull, kSiteSFull, kSitePFull, kSitePV, kSiteFinal, kSiteDrain };
 
 template <int D, int NSLOT>
 struct PairSmem {
@@ -49,8 +51,8 @@ struct PairSmem {
     static constexpr int kQOff = 0;
     static constexpr int kSlotOff = kTiles * kQBytes;
     static constexpr int kBarOff = kSlotOff + NSLOT * kSlotBytes;
-    // q_full, slot_full[NSLOT], slot_empty[NSLOT], per tile: s_full, s_free, p_full, pv_done; final, a_final
-    static constexpr int kNumBars = 1 + 2 * NSLOT + 4 * kTiles + 2;
+    // q_full, slot_full[NSLOT], slot_empty[NSLOT], per tile: s_full, p_full, pv_done; final, a_final
+    static constexpr int kNumBars = 1 + 2 * NSLOT + 3 * kTiles + 2;
     static constexpr int kTmemHolderOff = kBarOff + kNumBars * 8;
     static constexpr int kAlloc = kTmemHolderOff + 16 + 1024;
 };
@@ -62,9 +64,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     using L = PairSmem<D, NSLOT>;
     constexpr int kPanels = L::kPanels;
     constexpr uint32_t kTmemCols = 512;
-    // TMEM columns: S_A, S_B, P_A, P_B, then O_A, O_B
-    constexpr uint32_t kColS = 0, kColP = 2 * kBN, kColO = 256;
-    static_assert(kColP + kTiles * (kBN / 2) <= kColO && kColO + kTiles * D <= kTmemCols, "TMEM budget");
+    // TMEM columns: S_A, S_B (P_X over the first kBN/2 columns of S_X), then O_A, O_B
+    constexpr uint32_t kColS = 0, kColO = kTiles * kBN;
+    static_assert(kColO + kTiles * D <= kTmemCols, "TMEM budget");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -75,16 +77,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *slot_full = bars + 1;
     uint64_t *slot_empty = slot_full + NSLOT;
     uint64_t *s_full = slot_empty + NSLOT;  // [tile]: S_X(j) complete
-    uint64_t *s_free = s_full + kTiles;     // [tile]: softmax holds S_X(j) in registers
-    uint64_t *p_full = s_free + kTiles;     // [tile]: P_X(j) written (and O_X corrected)
+    uint64_t *p_full = s_full + kTiles;     // [tile]: P_X(j) written (and O_X corrected)
     uint64_t *pv_done = p_full + kTiles;    // [tile]: PV_X(j) complete
     uint64_t *final_bar = pv_done + kTiles; // issuer B: every PV MMA has completed
     uint64_t *a_final = final_bar + 1;      // issuer A: every S MMA has completed
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kTmemHolderOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int blk = gridDim.x - 1 - blockIdx.x;  // heaviest causal blocks first
-    const int bh = blockIdx.z * a.H + blockIdx.y;
+    const int n_blk = (a.N + kTiles * kBM - 1) / (kTiles * kBM);
+    int rank, bh;
+    tile_order(n_blk, a.B * a.H, a.causal, &rank, &bh);
+    const int blk = n_blk - 1 - rank;  // causal: the last block has the most keys
     const int N = a.N;
     const int row0 = blk * (kTiles * kBM);
     // K/V tiles query tile x needs (0 if the tile lies past N)
@@ -104,8 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int x = 0; x < kTiles; ++x) {
             mbar_init(&s_full[x], 1);
-            mbar_init(&s_free[x], 4);  // one arrive per softmax warp of tile x
-            mbar_init(&p_full[x], 4);
+            mbar_init(&p_full[x], 4);  // one arrive per softmax warp of tile x
             mbar_init(&pv_done[x], 1);
         }
         mbar_init(final_bar, 1);
@@ -175,8 +177,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int x = 0; x < kTiles; ++x) {
                 if (j >= (x == 0 ? n_kv0 : n_kv1)) continue;
-                // S_X is single-buffered: the softmax must hold S_X(j-1) in registers
-                if (j >= 1 && !(ok = warp_wait(&s_free[x], (j - 1) & 1, a.status, kSiteSFree))) break;
+                // S_X(j) overwrites P_X(j-1): PV_X(j-1) must have completed
+                if (j >= 1 && !(ok = warp_wait(&pv_done[x], (j - 1) & 1, a.status, kSitePV))) break;
                 tc_fence_after();
                 if (leader) {
 #pragma unroll
@@ -215,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (leader) {
 #pragma unroll
                     for (int kk = 0; kk < kBN / 16; ++kk)
-                        mma_ts(tmem + kColO + x * D, tmem + kColP + x * (kBN / 2) + kk * 8,
+                        mma_ts(tmem + kColO + x * D, tmem + kColS + x * kBN + kk * 8,
                                sdesc_add(v_desc, kk * 2048), idesc_o, (j > 0 || kk > 0));
                     mma_commit(&pv_done[x]);
                 }
@@ -236,41 +238,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tile_row0 = row0 + x * kBM;
         const int row = tile_row0 + r;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-        const uint32_t s_col = kColS + x * kBN, p_col = kColP + x * (kBN / 2), o_col = kColO + x * D;
+        const uint32_t s_col = kColS + x * kBN, o_col = kColO + x * D;
         const float c = a.scale_log2;
         const int n = x == 0 ? n_kv0 : n_kv1;
-        float m = -INFINITY, l = 0.f;
+        float m = -INFINITY, l = 0.f;  // running max (log2 units) and sum
         bool ok = true;
         for (int j = 0; j < n; ++j) {
+            // S_X(j) was issued after PV_X(j-1) completed, so O_X and the P columns are free as well
             ok = mbar_wait(&s_full[x], j & 1, a.status, kSiteSFull);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
-            float s[kBN];
-            {
-                uint32_t raw[kBN];
-                tmem_ld32(tmem + lane_base + s_col, raw);
-                tmem_ld32(tmem + lane_base + s_col + 32, raw + 32);
-                tmem_wait_ld();
-                tc_fence_before();
-                warp_arrive(&s_free[x]);  // S_X may be overwritten now
+            uint32_t raw[kBN];
 #pragma unroll
-                for (int i = 0; i < kBN; ++i) s[i] = __uint_as_float(raw[i]) * c;
-            }
+            for (int ch = 0; ch < kBN / 32; ++ch) tmem_ld32(tmem + lane_base + s_col + ch * 32, raw + ch * 32);
+            tmem_wait_ld();
             const int key0 = j * kBN;
             const bool need_mask = (key0 + kBN > N) || (a.causal && key0 + kBN - 1 > tile_row0);
             if (need_mask) {
                 const int lim = a.causal ? min(N - 1, row) : N - 1;  // last visible key
 #pragma unroll
                 for (int i = 0; i < kBN; ++i)
-                    if (key0 + i > lim) s[i] = -INFINITY;
+                    if (key0 + i > lim) raw[i] = 0xff800000u;  // -inf
             }
+            // row max of the raw scores (scale > 0 commutes with max)
             float mx[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) mx[u] = s[u];
+            for (int u = 0; u < 8; ++u) mx[u] = __uint_as_float(raw[u]);
 #pragma unroll
-            for (int i = 8; i < kBN; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
-            const float mt =
-                fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+            for (int i = 8; i < kBN; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(raw[i]));
+            const float mt = c * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
             const float m_new = fmaxf(m, mt);
             // Lazy correction: keep the stale max unless the row max grew by > 8 (factor 256).
             const bool need = m_new > m + 8.f;
@@ -278,23 +275,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float m_base = (m_use == -INFINITY) ? 0.f : m_use;
             const float alpha = need ? ex2_approx(m - m_base) : 1.f;
             float rsum[4] = {0.f, 0.f, 0.f, 0.f};
-            uint32_t pk[kBN / 2];
+            // P = 2^(s c - m) as bf16 pairs over the first kBN/2 columns of S_X, 32 columns per store
 #pragma unroll
-            for (int i = 0; i < kBN / 2; ++i) {
-                const float p0 = ex2_approx(s[2 * i] - m_base);
-                const float p1 = ex2_approx(s[2 * i + 1] - m_base);
-                rsum[i & 3] += p0 + p1;
-                pk[i] = pack_bf16x2(p0, p1);
+            for (int h = 0; h < kBN / 64; ++h) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(raw[64 * h + 2 * i]), c, -m_base));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(raw[64 * h + 2 * i + 1]), c, -m_base));
+                    rsum[i & 3] += p0 + p1;
+                    pk[i] = pack_bf16x2(p0, p1);
+                }
+                tmem_st32(tmem + lane_base + s_col + h * 32, pk);
             }
             l = l * alpha + ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3]));
             m = m_use;
-            // P_X and O_X were last touched by PV_X(j-1)
-            if (j >= 1) {
-                ok = mbar_wait(&pv_done[x], (j - 1) & 1, a.status, kSitePV);
-                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                tc_fence_after();
-            }
-            tmem_st32(tmem + lane_base + p_col, pk);
             if (j >= 1 && __any_sync(0xffffffffu, need)) {
                 uint32_t ov[32];
 #pragma unroll
@@ -356,7 +351,7 @@ cudaError_t launch_spec(const FwdArgs &a, const CUtensorMap &tq, const CUtensorM
     auto kern = fwd_bf16_pair_kernel<D, NSLOT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
-    dim3 grid((a.N + kTiles * kBM - 1) / (kTiles * kBM), a.H, a.B);
+    dim3 grid(((a.N + kTiles * kBM - 1) / (kTiles * kBM)) * a.H * a.B);
     kern<<<grid, kThreads, L::kAlloc, s>>>(tq, tk, tv, a);
     return cudaGetLastError();
 }
@@ -366,8 +361,8 @@ cudaError_t launch_spec(const FwdArgs &a, const CUtensorMap &tq, const CUtensorM
 cudaError_t launch_fwd_bf16_pair(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
                                  const CUtensorMap &tv, cudaStream_t s) {
     switch (a.D) {
-        case 64: return launch_spec<64, 12>(a, tq, tk, tv, s);
-        case 128: return launch_spec<128, 8>(a, tq, tk, tv, s);
+        case 64: return launch_spec<64, 10>(a, tq, tk, tv, s);
+        case 128: return launch_spec<128, 5>(a, tq, tk, tv, s);
         default: return cudaErrorInvalidValue;
     }
 }

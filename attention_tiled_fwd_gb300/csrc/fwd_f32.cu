@@ -43,8 +43,9 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_f32_kernel(FwdArgs a) {
     float *k_s = q_s + kBM * D;           // [kBN][D + 1]
     float *v_s = k_s + kBN * (D + 1);     // [kBN][D]
 
-    const int q_tile = gridDim.x - 1 - blockIdx.x;  // heaviest causal tiles first
-    const int bh = blockIdx.z * a.H + blockIdx.y;
+    int rank, bh;
+    tile_order((a.N + kBM - 1) / kBM, a.B * a.H, a.causal, &rank, &bh);
+    const int q_tile = (a.N + kBM - 1) / kBM - 1 - rank;  // causal: the last query tile has the most keys
     const int N = a.N;
     const float *q = static_cast<const float *>(a.q) + (size_t)bh * N * D;
     const float *k = static_cast<const float *>(a.k) + (size_t)bh * N * D;
@@ -124,7 +125,7 @@ cudaError_t launch_dpl(const FwdArgs &a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(fwd_f32_kernel<DPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((a.N + kBM - 1) / kBM, a.H, a.B);
+    dim3 grid(((a.N + kBM - 1) / kBM) * a.H * a.B);
     fwd_f32_kernel<DPL><<<grid, kWarps * 32, smem, s>>>(a);
     return cudaGetLastError();
 }
