@@ -13,7 +13,9 @@ namespace fa {
 // exceed) shared memory.
 //   D = 64, 128: two 128-row query tiles per CTA (fwd_bf16_pair.cu); TMEM per
 //                tile S 128 (P over its first 64) + O D columns; shared memory
-//                2 Q tiles + ring.
+//                2 Q tiles + ring.  Non-causal D = 128 instead runs the
+//                one-tile kernel of fwd_bf16.cu with 128-key tiles (S
+//                double-buffered, 5-slot ring), which measured faster there.
 //   D = 256:     one 128-row query tile, two softmax warpgroups splitting the
 //                columns (fwd_bf16.cu); TMEM S 2x64 + P 2x32 + O 256 (one
 //                N = 256 accumulator, D-blocked shared-memory panels).

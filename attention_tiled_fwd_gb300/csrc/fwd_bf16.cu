@@ -1,8 +1,9 @@
-// fwd_bf16.cu -- bf16 attention forward on the 5th-generation tensor cores,
-// one 128-row query tile per CTA; used for D = 256 (D = 64 and 128 run the
-// two-tile kernel of fwd_bf16_pair.cu, which does not fit D = 256 in TMEM)
-// (tcgen05, accumulators in TMEM), K/V tiles streamed by TMA through an
-// mbarrier ring in shared memory.
+// fwd_bf16.cu -- bf16 attention forward on the 5th-generation tensor cores
+// (tcgen05, accumulators in TMEM), one 128-row query tile per CTA, K/V tiles
+// streamed by TMA through an mbarrier ring in shared memory.  Used for
+// D = 256 (64-key tiles) and for non-causal D = 128 (128-key tiles); the
+// other cases run the two-tile kernel of fwd_bf16_pair.cu (launch_fwd_bf16
+// below holds the measured choice).
 //
 // Algorithm ("Learning Metal with FlashAttention", section "FlashAttention";
 // metalworking "Flash Attention", kernel anatomy items 1-5; metal-flash-
@@ -248,32 +249,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = mbar_wait(&s_full[j & 1], (j >> 1) & 1, a.status, kSiteSFull);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
-            float s[HB];
-            {
-                uint32_t raw[32];
+            // raw scores; the scale is folded into the exponent's FMA below
+            uint32_t raw[HB];
 #pragma unroll
-                for (int ch = 0; ch < HB / 32; ++ch) {
-                    tmem_ld32(tmem + lane_base + s_col + ch * 32, raw);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) s[ch * 32 + i] = __uint_as_float(raw[i]) * c;
-                }
-            }
+            for (int ch = 0; ch < HB / 32; ++ch) tmem_ld32(tmem + lane_base + s_col + ch * 32, raw + ch * 32);
+            tmem_wait_ld();
             const int key0 = j * BN + g * HB;
             const bool need_mask = (key0 + HB > N) || (a.causal && key0 + HB - 1 > q_tile * kBM);
             if (need_mask) {
                 const int lim = a.causal ? min(N - 1, row) : N - 1;  // last visible key
 #pragma unroll
                 for (int i = 0; i < HB; ++i)
-                    if (key0 + i > lim) s[i] = -INFINITY;
+                    if (key0 + i > lim) raw[i] = 0xff800000u;  // -inf
             }
-            // row max over this half: 8 independent partial maxima, then a small tree
-            float mx[8];
+            // row max over this half (scale > 0 commutes with max): four chains of three-input maxima
+            float mx[4];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) mx[u] = s[u];
+            for (int u = 0; u < 4; ++u) mx[u] = __uint_as_float(raw[u]);
 #pragma unroll
-            for (int i = 8; i < HB; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
-            float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+            for (int i = 4; i + 8 <= HB; i += 8)
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    mx[u] = fmax3(mx[u], __uint_as_float(raw[i + 2 * u]), __uint_as_float(raw[i + 2 * u + 1]));
+#pragma unroll
+            for (int u = 0; u < 4; ++u) mx[u] = fmaxf(mx[u], __uint_as_float(raw[HB - 4 + u]));
+            float mt = c * fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
             // combine with the other half of the row
             smax[((j & 1) * 2 + g) * kBM + r] = mt;
             warp_arrive(&xchg[j & 1]);
@@ -286,31 +286,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float m_use = need ? m_new : m;
             const float m_base = (m_use == -INFINITY) ? 0.f : m_use;
             const float alpha = need ? ex2_approx(m - m_base) : 1.f;
-            float rsum[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial row sums
             // P[j % 2] was last read by PV_{j-2}
             if (j >= 2) {
                 ok = mbar_wait(&pv_done[j & 1], ((j >> 1) - 1) & 1, a.status, kSitePV);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc_fence_after();
             }
-            // P = 2^(S - m) as bf16 pairs into this tile's P buffer (this half's columns).
-            constexpr int kPk = HB >= 64 ? 32 : HB / 2;  // packed pairs per store (32 or 16 columns)
+            // P = 2^(s c - m) as bf16 pairs into this tile's P buffer (this half's columns), 16 columns
+            // per store; the scaling FMA and the row sum run on fp32 pairs
+            const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(-m_base, -m_base);
+            uint64_t acc2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
-            for (int ch = 0; ch < HB / (2 * kPk); ++ch) {
-                uint32_t pk[kPk];
+            for (int ch = 0; ch < HB / 32; ++ch) {
+                uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < kPk; ++i) {
-                    const float p0 = ex2_approx(s[ch * 64 + 2 * i] - m_base);
-                    const float p1 = ex2_approx(s[ch * 64 + 2 * i + 1] - m_base);
-                    rsum[i & 3] += p0 + p1;
+                for (int i = 0; i < 16; ++i) {
+                    const uint64_t y2 = f2_fma(f2_pack(__uint_as_float(raw[ch * 32 + 2 * i]),
+                                                       __uint_as_float(raw[ch * 32 + 2 * i + 1])), c2, nm2);
+                    float y0, y1;
+                    f2_unpack(y2, y0, y1);
+                    const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
+                    acc2[i & 1] = f2_add(acc2[i & 1], f2_pack(p0, p1));
                     pk[i] = pack_bf16x2(p0, p1);
                 }
-                if constexpr (kPk == 32)
-                    tmem_st32(tmem + lane_base + p_col + ch * 32, pk);
-                else
-                    tmem_st16(tmem + lane_base + p_col + ch * 32, pk);
+                tmem_st16(tmem + lane_base + p_col + ch * 16, pk);
             }
-            l = l * alpha + ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3]));
+            float r0, r1, r2, r3;
+            f2_unpack(acc2[0], r0, r1);
+            f2_unpack(acc2[1], r2, r3);
+            l = l * alpha + ((r0 + r1) + (r2 + r3));
             m = m_use;
             if (j > 0 && __any_sync(0xffffffffu, need)) {
                 // O must hold P_{j-1} V_{j-1} before it is rescaled (this half's columns).
@@ -397,8 +401,12 @@ cudaError_t launch_spec(const FwdArgs &a, const CUtensorMap &tq, const CUtensorM
 cudaError_t launch_fwd_bf16(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             cudaStream_t s) {
     switch (a.D) {
-        case 64:
-        case 128: return launch_fwd_bf16_pair(a, tq, tk, tv, s);  // two query tiles per CTA
+        // measured choice per head dimension and mask: the two-tile kernel amortises its
+        // pipeline fill over twice the rows (better for causal launches, whose CTAs are short,
+        // and for D = 64, where the softmax dominates); the one-tile kernel double-buffers S
+        // (better for long non-causal rows at D = 128)
+        case 64: return launch_fwd_bf16_pair(a, tq, tk, tv, s);
+        case 128: return a.causal ? launch_fwd_bf16_pair(a, tq, tk, tv, s) : launch_spec<128, 128, 5>(a, tq, tk, tv, s);
         case 256: return launch_spec<256, 64, 4>(a, tq, tk, tv, s);
         default: return cudaErrorInvalidValue;
     }

@@ -9,13 +9,12 @@
 //
 // GB300 mapping (why a pair): one softmax warpgroup owns each query tile, so a
 // thread owns a whole row (its TMEM lane) and the row max / sum are
-// thread-local -- no exchange between warps -- while the two warpgroups run
-// out of phase: the tensor core works on one tile's S or PV while the other
-// tile's softmax runs.
+// thread-local -- no exchange between warps -- and the tensor core works on
+// one tile's S or PV while the other tile's softmax runs.
 //   warp 0      TMA producer: Q_A, Q_B once, then K_j, V_j (128 rows) into a ring
-//   warp 1      TMEM allocator + tcgen05 issuer of S_X = Q_X K_j^T (X = A, B)
-//   warp 2      tcgen05 issuer of O_X += P_X V_j
-//   warps 3-6   softmax of tile A; warps 7-10 softmax of tile B
+//   warp 1      TMEM allocator + the one tcgen05 issuer, in the fixed order
+//                 S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ...
+//   warps 2-5   softmax of tile A; warps 6-9 softmax of tile B
 // TMEM (512 columns): S_A, S_B (128 fp32 columns each), O_A, O_B (D columns
 // each).  128-key tiles keep the S MMA at N = 128, where it runs at the full
 // tensor rate (at N = 64 it is shared-memory-bound).  P_X(j) is written as
@@ -38,7 +37,7 @@ namespace {
 constexpr int kBM = 128;            // rows per query tile (TMEM lanes)
 constexpr int kBN = 128;            // keys per K/V tile
 constexpr int kTiles = 2;           // query tiles per CTA
-constexpr int kFirstSoftmaxWarp = 3;
+constexpr int kFirstSoftmaxWarp = 2;
 constexpr int kThreads = 32 * kFirstSoftmaxWarp + 128 * kTiles;
 
 enum : int { kSiteQ = 61, kSiteSlotEmpty, kSiteSlotFull, kSiteSFull, kSitePFull, kSitePV, kSiteFinal, kSiteDrain };
@@ -51,8 +50,8 @@ struct PairSmem {
     static constexpr int kQOff = 0;
     static constexpr int kSlotOff = kTiles * kQBytes;
     static constexpr int kBarOff = kSlotOff + NSLOT * kSlotBytes;
-    // q_full, slot_full[NSLOT], slot_empty[NSLOT], per tile: s_full, p_full, pv_done; final, a_final
-    static constexpr int kNumBars = 1 + 2 * NSLOT + 3 * kTiles + 2;
+    // q_full, slot_full[NSLOT], slot_empty[NSLOT], per tile: s_full, p_full, pv_done; final
+    static constexpr int kNumBars = 1 + 2 * NSLOT + 3 * kTiles + 1;
     static constexpr int kTmemHolderOff = kBarOff + kNumBars * 8;
     static constexpr int kAlloc = kTmemHolderOff + 16 + 1024;
 };
@@ -79,8 +78,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *s_full = slot_empty + NSLOT;  // [tile]: S_X(j) complete
     uint64_t *p_full = s_full + kTiles;     // [tile]: P_X(j) written (and O_X corrected)
     uint64_t *pv_done = p_full + kTiles;    // [tile]: PV_X(j) complete
-    uint64_t *final_bar = pv_done + kTiles; // issuer B: every PV MMA has completed
-    uint64_t *a_final = final_bar + 1;      // issuer A: every S MMA has completed
+    uint64_t *final_bar = pv_done + kTiles; // every MMA of the CTA has completed
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kTmemHolderOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -111,7 +109,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&pv_done[x], 1);
         }
         mbar_init(final_bar, 1);
-        mbar_init(a_final, 1);
         fence_mbarrier_init();
     }
     if (warp == 1) {
@@ -160,73 +157,71 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------------------------------------ issuer A: S_X(j) = Q_X K_j^T
+        // ------------------------------------------------------------ the tcgen05 issuer
         // The whole warp runs the loop (operands stay warp-uniform); one elected lane issues the MMAs
         // and the commits that track them.
         constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, false, false);
+        constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, false, true);
         const uint64_t q_desc = sdesc_sw128(smem_u32(q_s), 16, 1024);
         const uint32_t slot_addr = smem_u32(slots);
         const bool leader = elect_one();
         bool ok = warp_wait(q_full, 0, a.status, kSiteQ);
         tc_fence_after();
-        for (int j = 0; ok && j < n_all; ++j) {
-            const int slot = (2 * j) % NSLOT, round = (2 * j) / NSLOT;
-            if (!(ok = warp_wait(&slot_full[slot], round & 1, a.status, kSiteSlotFull))) break;
+        // S_X(j) = Q_X K_j^T into S_X; K_j is in slot 2j mod NSLOT
+        auto issue_s = [&](int x, int j) {
+            if (!ok || j >= (x == 0 ? n_kv0 : n_kv1)) return;
+            const int slot = (2 * j) % NSLOT;
+            if (!(ok = warp_wait(&slot_full[slot], ((2 * j) / NSLOT) & 1, a.status, kSiteSlotFull))) return;
+            // S_X(j) overwrites P_X(j-1): PV_X(j-1) must have completed
+            if (j >= 1 && !(ok = warp_wait(&pv_done[x], (j - 1) & 1, a.status, kSitePV))) return;
             tc_fence_after();
             const uint64_t k_desc = sdesc_sw128(slot_addr + slot * L::kSlotBytes, 16, 1024);
+            if (leader) {
 #pragma unroll
-            for (int x = 0; x < kTiles; ++x) {
-                if (j >= (x == 0 ? n_kv0 : n_kv1)) continue;
-                // S_X(j) overwrites P_X(j-1): PV_X(j-1) must have completed
-                if (j >= 1 && !(ok = warp_wait(&pv_done[x], (j - 1) & 1, a.status, kSitePV))) break;
-                tc_fence_after();
-                if (leader) {
-#pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint32_t off = (ks >> 2) * (kBM * 128) + (ks & 3) * 32;
-                        mma_ss(tmem + kColS + x * kBN, sdesc_add(q_desc, x * L::kQBytes + off),
-                               sdesc_add(k_desc, (ks >> 2) * (kBN * 128) + (ks & 3) * 32), idesc_s, ks > 0);
-                    }
-                    mma_commit(&s_full[x]);
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks >> 2) * (kBM * 128) + (ks & 3) * 32;
+                    mma_ss(tmem + kColS + x * kBN, sdesc_add(q_desc, x * L::kQBytes + off),
+                           sdesc_add(k_desc, (ks >> 2) * (kBN * 128) + (ks & 3) * 32), idesc_s, ks > 0);
                 }
-                __syncwarp();
+                mma_commit(&s_full[x]);
             }
-            if (!ok) break;
-            if (leader) mma_commit(&slot_empty[slot]);  // K_j read by both S MMAs
             __syncwarp();
-        }
-        // Drain this warp's MMAs before TMEM can be released (immediate in the normal path).
-        if (leader) mma_commit(a_final);
-        __syncwarp();
-        warp_wait(a_final, 0, a.status, kSiteFinal);
-    } else if (warp == 2) {
-        // ------------------------------------------------------------ issuer B: O_X += P_X(j) V_j
-        constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, false, true);
-        const uint32_t slot_addr = smem_u32(slots);
-        const bool leader = elect_one();
-        bool ok = true;
-        for (int j = 0; ok && j < n_all; ++j) {
-            const int slot = (2 * j + 1) % NSLOT, round = (2 * j + 1) / NSLOT;
-            if (!(ok = warp_wait(&slot_full[slot], round & 1, a.status, kSiteSlotFull))) break;
+        };
+        // O_X += P_X(j) V_j, P_X from TMEM; V_j is in slot 2j+1 mod NSLOT
+        auto issue_pv = [&](int x, int j) {
+            if (!ok || j >= (x == 0 ? n_kv0 : n_kv1)) return;
+            const int slot = (2 * j + 1) % NSLOT;
+            if (!(ok = warp_wait(&slot_full[slot], ((2 * j + 1) / NSLOT) & 1, a.status, kSiteSlotFull))) return;
+            if (!(ok = warp_wait(&p_full[x], j & 1, a.status, kSitePFull))) return;
+            tc_fence_after();
             const uint64_t v_desc = sdesc_sw128(slot_addr + slot * L::kSlotBytes, kBN * 128, 1024);
+            if (leader) {
 #pragma unroll
-            for (int x = 0; x < kTiles; ++x) {
-                if (j >= (x == 0 ? n_kv0 : n_kv1)) continue;
-                if (!(ok = warp_wait(&p_full[x], j & 1, a.status, kSitePFull))) break;
-                tc_fence_after();
-                if (leader) {
-#pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk)
-                        mma_ts(tmem + kColO + x * D, tmem + kColS + x * kBN + kk * 8,
-                               sdesc_add(v_desc, kk * 2048), idesc_o, (j > 0 || kk > 0));
-                    mma_commit(&pv_done[x]);
-                }
-                __syncwarp();
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    mma_ts(tmem + kColO + x * D, tmem + kColS + x * kBN + kk * 8, sdesc_add(v_desc, kk * 2048),
+                           idesc_o, (j > 0 || kk > 0));
+                mma_commit(&pv_done[x]);
             }
-            if (!ok) break;
-            if (leader) mma_commit(&slot_empty[slot]);  // V_j read by both PV MMAs
             __syncwarp();
+        };
+        // a slot is released by a commit after the last MMA that reads it (a commit tracks every
+        // earlier MMA of this thread)
+        auto release = [&](int idx) {
+            if (leader) mma_commit(&slot_empty[idx % NSLOT]);
+            __syncwarp();
+        };
+        issue_s(0, 0);
+        issue_s(1, 0);
+        if (ok) release(0);
+        for (int j = 0; ok && j < n_all; ++j) {
+            issue_pv(0, j);
+            issue_s(0, j + 1);
+            issue_pv(1, j);
+            if (ok) release(2 * j + 1);  // V_j
+            issue_s(1, j + 1);
+            if (ok && j + 1 < n_all) release(2 * j + 2);  // K_{j+1}
         }
+        // every MMA complete: the epilogue may read O, and TMEM may be released
         if (leader) mma_commit(final_bar);
         __syncwarp();
         warp_wait(final_bar, 0, a.status, kSiteFinal);
@@ -260,35 +255,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < kBN; ++i)
                     if (key0 + i > lim) raw[i] = 0xff800000u;  // -inf
             }
-            // row max of the raw scores (scale > 0 commutes with max)
-            float mx[8];
+            // row max of the raw scores (scale > 0 commutes with max): four chains of three-input maxima
+            float mx[4];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) mx[u] = __uint_as_float(raw[u]);
+            for (int u = 0; u < 4; ++u) mx[u] = __uint_as_float(raw[u]);
 #pragma unroll
-            for (int i = 8; i < kBN; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(raw[i]));
-            const float mt = c * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+            for (int i = 4; i + 8 <= kBN; i += 8)
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    mx[u] = fmax3(mx[u], __uint_as_float(raw[i + 2 * u]), __uint_as_float(raw[i + 2 * u + 1]));
+#pragma unroll
+            for (int u = 0; u < 4; ++u) mx[u] = fmaxf(mx[u], __uint_as_float(raw[kBN - 4 + u]));
+            const float mt = c * fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
             const float m_new = fmaxf(m, mt);
             // Lazy correction: keep the stale max unless the row max grew by > 8 (factor 256).
             const bool need = m_new > m + 8.f;
             const float m_use = need ? m_new : m;
             const float m_base = (m_use == -INFINITY) ? 0.f : m_use;
             const float alpha = need ? ex2_approx(m - m_base) : 1.f;
-            float rsum[4] = {0.f, 0.f, 0.f, 0.f};
-            // P = 2^(s c - m) as bf16 pairs over the first kBN/2 columns of S_X, 32 columns per store
+            // P = 2^(s c - m) as bf16 pairs over the first kBN/2 columns of S_X, 16 columns per store;
+            // the scaling FMA and the row sum run on fp32 pairs
+            const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(-m_base, -m_base);
+            uint64_t acc2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
-            for (int h = 0; h < kBN / 64; ++h) {
-                uint32_t pk[32];
+            for (int h = 0; h < kBN / 32; ++h) {
+                uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(raw[64 * h + 2 * i]), c, -m_base));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(raw[64 * h + 2 * i + 1]), c, -m_base));
-                    rsum[i & 3] += p0 + p1;
+                for (int i = 0; i < 16; ++i) {
+                    const uint64_t y2 = f2_fma(f2_pack(__uint_as_float(raw[32 * h + 2 * i]),
+                                                       __uint_as_float(raw[32 * h + 2 * i + 1])), c2, nm2);
+                    float y0, y1;
+                    f2_unpack(y2, y0, y1);
+                    const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
+                    acc2[i & 1] = f2_add(acc2[i & 1], f2_pack(p0, p1));
                     pk[i] = pack_bf16x2(p0, p1);
                 }
-                tmem_st32(tmem + lane_base + s_col + h * 32, pk);
+                tmem_st16(tmem + lane_base + s_col + h * 16, pk);
             }
-            l = l * alpha + ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3]));
+            float r0, r1, r2, r3;
+            f2_unpack(acc2[0], r0, r1);
+            f2_unpack(acc2[1], r2, r3);
+            l = l * alpha + ((r0 + r1) + (r2 + r3));
             m = m_use;
             if (j >= 1 && __any_sync(0xffffffffu, need)) {
                 uint32_t ov[32];
