@@ -79,7 +79,8 @@ def source_hash(paths) -> str:
 
 
 KERNEL_SOURCES = {
-    "fwd": ["attention_tiled_fwd_gb300/csrc/fwd_bf16.cu", "attention_tiled_fwd_gb300/csrc/sm100_ptx.cuh"],
+    "fwd": ["attention_tiled_fwd_gb300/csrc/fwd_bf16.cu", "attention_tiled_fwd_gb300/csrc/fwd_bf16_pair.cu",
+            "attention_tiled_fwd_gb300/csrc/sm100_ptx.cuh"],
     "bwd_dq": ["attention_tiled_fwd_gb300/csrc/bwd_dq.cu", "attention_tiled_fwd_gb300/csrc/sm100_ptx.cuh"],
     "bwd_dkdv": ["attention_tiled_fwd_gb300/csrc/bwd_dkdv.cu", "attention_tiled_fwd_gb300/csrc/sm100_ptx.cuh"],
 }
