@@ -22,7 +22,8 @@ from ._native import FA_BF16, FA_F32, FAError
 
 __all__ = ["fa_forward", "fa_backward_dq", "fa_backward_dkdv", "fa_decode", "fa_decode_workspace_bytes",
            "fa_decode_noalloc",
-           "fa_device_status", "fa_selftest_timeout", "FAError", "FA_BF16", "FA_F32", "attention_flops"]
+           "fa_device_status", "fa_selftest_timeout", "FAError", "FA_BF16", "FA_F32", "attention_flops",
+           "attention"]
 
 _DT = {torch.bfloat16: FA_BF16, torch.float32: FA_F32}
 
@@ -182,3 +183,6 @@ def attention_flops(B: int, H: int, N: int, D: int, causal: bool, pass_: str = "
     per = {"fwd": 4.0, "bwd": 14.0, "bwd_dq": 6.0, "bwd_dkdv": 8.0}[pass_]
     f = per * B * H * float(N) * N * D
     return f / 2 if causal else f
+
+
+from .autograd import attention  # noqa: E402  (differentiable wrapper over the functions above)

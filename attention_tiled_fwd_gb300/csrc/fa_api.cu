@@ -39,6 +39,10 @@ int device_state(int *dev_out, DeviceState **st_out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return FA_ERR_DEVICE;
+    // Bind the device's primary context to the calling thread: a thread that has made no runtime
+    // call yet (a worker thread, autograd's backward thread) has no current context, and the
+    // tensor-map encoder is a driver call that needs one.
+    if (cudaSetDevice(dev) != cudaSuccess) return FA_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceState &st = g_dev[dev];
     if (!st.ready) {
@@ -125,7 +129,7 @@ extern "C" int fa_forward(const void *q, const void *k, const void *v, void *o, 
     int rc = check_shape(B, H, N, D, scale);
     if (rc != FA_OK) return rc;
     if (dtype == FA_BF16) {
-        if (D != 64 && D != 128 && D != 256) return FA_ERR_HEAD_DIM;
+        if (D != 64 && D != 128 && D != 192 && D != 256) return FA_ERR_HEAD_DIM;
     } else if (dtype == FA_F32) {
         if (D % 32 != 0 || D > 256) return FA_ERR_HEAD_DIM;
     } else {

@@ -16,15 +16,16 @@ namespace fa {
 //                2 Q tiles + ring.  Non-causal D = 128 instead runs the
 //                one-tile kernel of fwd_bf16.cu with 128-key tiles (S
 //                double-buffered, 5-slot ring), which measured faster there.
-//   D = 256:     one 128-row query tile, two softmax warpgroups splitting the
-//                columns (fwd_bf16.cu); TMEM S 2x64 + P 2x32 + O 256 (one
-//                N = 256 accumulator, D-blocked shared-memory panels).
+//   D = 192, 256: one 128-row query tile, two softmax warpgroups splitting
+//                the columns (fwd_bf16.cu); TMEM S 2x64 + P 2x32 + O D (one
+//                N = D accumulator, D-blocked shared-memory panels).
 struct FwdSpec {
     int D, BM, BN, nslot;
 };
 constexpr FwdSpec kFwdSpecs[] = {
     {64, 256, 128, 10},  // Q 2 x 16 KB + 10 x 16 KB ring
     {128, 256, 128, 5},  // Q 2 x 32 KB + 5 x 32 KB ring
+    {192, 128, 64, 7},  // Q 48 KB + 7 x 24 KB ring
     {256, 128, 64, 4},  // Q 64 KB + 4 x 32 KB ring
 };
 

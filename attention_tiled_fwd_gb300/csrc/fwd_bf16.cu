@@ -1,7 +1,7 @@
 // fwd_bf16.cu -- bf16 attention forward on the 5th-generation tensor cores
 // (tcgen05, accumulators in TMEM), one 128-row query tile per CTA, K/V tiles
 // streamed by TMA through an mbarrier ring in shared memory.  Used for
-// D = 256 (64-key tiles) and for non-causal D = 128 (128-key tiles); the
+// D = 192 and 256 (64-key tiles) and for non-causal D = 128 (128-key tiles); the
 // other cases run the two-tile kernel of fwd_bf16_pair.cu (launch_fwd_bf16
 // below holds the measured choice).
 //
@@ -407,6 +407,7 @@ cudaError_t launch_fwd_bf16(const FwdArgs &a, const CUtensorMap &tq, const CUten
         // (better for long non-causal rows at D = 128)
         case 64: return launch_fwd_bf16_pair(a, tq, tk, tv, s);
         case 128: return a.causal ? launch_fwd_bf16_pair(a, tq, tk, tv, s) : launch_spec<128, 128, 5>(a, tq, tk, tv, s);
+        case 192: return launch_spec<192, 64, 7>(a, tq, tk, tv, s);
         case 256: return launch_spec<256, 64, 4>(a, tq, tk, tv, s);
         default: return cudaErrorInvalidValue;
     }

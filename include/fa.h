@@ -75,7 +75,7 @@ enum fa_status {
 /*
  * fa_forward -- O = softmax(scale Q K^T) V and LSE (natural log-sum-exp of the
  * scaled scores of each row).
- *   dtype FA_BF16: D in {64, 128, 256}; bf16 inputs, fp32 accumulation
+ *   dtype FA_BF16: D in {64, 128, 192, 256}; bf16 inputs, fp32 accumulation
  *                  (tcgen05 tensor cores), bf16 O, fp32 LSE.
  *   dtype FA_F32 : D a multiple of 32 in [32, 256]; fp32 inputs and O,
  *                  fp32 FFMA arithmetic throughout, fp32 LSE.

@@ -51,7 +51,8 @@ def test_fp32_forward_edge_shapes(shape, causal):
 
 # Several query and key tiles, ragged tails (N not a multiple of 128 or 64), N < tile, N = 1.
 BF16_SHAPES = [(1, 1, 1, 64), (1, 2, 77, 64), (1, 1, 128, 128), (2, 2, 300, 64), (1, 2, 257, 128),
-               (1, 1, 383, 128), (1, 1, 129, 256), (1, 2, 320, 256), (2, 1, 640, 128)]
+               (1, 1, 383, 128), (1, 1, 129, 256), (1, 2, 320, 256), (2, 1, 640, 128), (1, 1, 65, 192),
+               (1, 2, 333, 192)]
 
 
 @pytest.mark.parametrize("shape", BF16_SHAPES)
@@ -95,7 +96,8 @@ def test_bf16_forward_increasing_logits_force_rescale():
         assert_close(to_np(lse), rl, TOL_LSE, what="bf16 LSE rising max")
 
 
-@pytest.mark.parametrize("shape", [(1, 2, 320, 256), (2, 2, 448, 256), (1, 4, 1000, 64), (1, 2, 1152, 128)])
+@pytest.mark.parametrize("shape", [(1, 2, 320, 256), (2, 2, 448, 256), (1, 4, 1000, 64), (1, 2, 1152, 128),
+                                   (1, 2, 1000, 192)])
 def test_bf16_forward_repeated_many_tiles(shape):
     """Many K/V tiles per CTA, non-causal and causal, several runs: catches pipeline races whose
     outcome depends on the relative speed of the MMA issuer and the softmax warps."""

@@ -33,7 +33,7 @@ def test_forward_rejects_bad_shapes(lib):
 
 
 def test_forward_rejects_head_dims(lib):
-    for D in (0, 16, 32, 96, 100, 192, 512):
+    for D in (0, 16, 32, 96, 100, 160, 320, 512):
         assert fwd(lib, D=D) in (nat.FA_ERR_HEAD_DIM, nat.FA_ERR_SHAPE), D
     for D in (48, 100, 288):
         assert fwd(lib, D=D, dtype=nat.FA_F32) == nat.FA_ERR_HEAD_DIM, D
@@ -111,3 +111,37 @@ def test_bounded_wait_times_out_and_reports(lib):
     assert fa.fa_device_status() == 0  # read clears it
     x = torch.ones(1024, device=dev)
     assert float(x.sum()) == 1024.0
+
+
+@pytest.mark.gpu
+def test_calls_from_a_fresh_thread():
+    """Every entry point works from a thread that has made no CUDA call before (a worker thread,
+    or autograd's backward thread)."""
+    import threading
+    import torch
+    import attention_tiled_fwd_gb300 as fa
+    from helpers import cuda_or_skip
+    dev = cuda_or_skip()
+    g = torch.Generator().manual_seed(5)
+    q, k, v, dO = (torch.randn(1, 2, 200, 64, generator=g).bfloat16().to(dev) for _ in range(4))
+    o_main, lse_main = fa.fa_forward(q, k, v, causal=True)
+    out = {}
+
+    def work():
+        try:
+            o, lse = fa.fa_forward(q, k, v, causal=True)
+            dq, delta = fa.fa_backward_dq(q, k, v, o, dO, lse, causal=True, grad_dtype=torch.bfloat16)
+            dk, dv = fa.fa_backward_dkdv(q, k, v, dO, lse, delta, causal=True, grad_dtype=torch.bfloat16)
+            od, _ = fa.fa_decode(q[:, :, -1:].contiguous(), k, v, causal=True)
+            torch.cuda.synchronize()
+            out["r"] = (o, od)
+        except Exception as e:  # reported in the main thread
+            out["e"] = e
+
+    th = threading.Thread(target=work)
+    th.start()
+    th.join()
+    assert "e" not in out, out.get("e")
+    o, od = out["r"]
+    assert torch.equal(o, o_main)
+    assert (od.float() - o_main[:, :, -1:].float()).abs().max().item() < 2e-2
