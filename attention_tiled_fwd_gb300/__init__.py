@@ -20,7 +20,7 @@ import torch
 from . import _native
 from ._native import FA_BF16, FA_F32, FAError
 
-__all__ = ["fa_forward", "fa_backward_dq", "fa_backward_dkdv", "fa_decode", "fa_decode_workspace_bytes",
+__all__ = ["fa_forward", "fa_backward_dq", "fa_backward_dkdv", "fa_backward_atomic", "fa_decode", "fa_decode_workspace_bytes",
            "fa_decode_noalloc",
            "fa_device_status", "fa_selftest_timeout", "FAError", "FA_BF16", "FA_F32", "attention_flops",
            "attention"]
@@ -111,6 +111,37 @@ def fa_backward_dkdv(q, k, v, dO, lse, delta, scale: Optional[float] = None, cau
                               _dtype_code(dk), _stream_ptr(stream))
     _native.check(rc, "fa_backward_dkdv")
     return dk, dv
+
+
+def fa_backward_atomic(q, k, v, o, dO, lse, scale: Optional[float] = None, causal: bool = False,
+                       grad_dtype: torch.dtype = torch.float32, dq_accum: Optional[torch.Tensor] = None,
+                       dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None,
+                       dv: Optional[torch.Tensor] = None, delta: Optional[torch.Tensor] = None,
+                       stream: Optional[torch.cuda.Stream] = None):
+    """The 5-GEMM comparator backward (fa_backward_atomic).  Returns (dq, dk, dv, delta).
+
+    dq_accum is an fp32 CUDA tensor of at least B*H*N*D elements; outputs and dq_accum are
+    allocated here when the caller passes none (dq, dk, dv in grad_dtype unless given)."""
+    B, H, N, D = _shape4(q, "q")
+    if dq is None:
+        dq = torch.empty((B, H, N, D), dtype=grad_dtype, device=q.device)
+    if dk is None:
+        dk = torch.empty_like(dq)
+    if dv is None:
+        dv = torch.empty_like(dq)
+    if not (dq.dtype == dk.dtype == dv.dtype):
+        raise ValueError("dq, dk and dv must share a dtype")
+    if delta is None:
+        delta = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if dq_accum is None:
+        dq_accum = torch.empty((B, H, N, D), dtype=torch.float32, device=q.device)
+    lib = _native.load()
+    rc = lib.fa_backward_atomic(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(delta), _ptr(dq),
+                                _ptr(dk), _ptr(dv), _ptr(dq_accum), dq_accum.numel() * dq_accum.element_size(),
+                                B, H, N, D, _scale(scale, D), int(bool(causal)), _dtype_code(q), _dtype_code(dq),
+                                _stream_ptr(stream))
+    _native.check(rc, "fa_backward_atomic")
+    return dq, dk, dv, delta
 
 
 def fa_decode_workspace_bytes(B: int, H: int, n_q: int, N: int, D: int) -> int:

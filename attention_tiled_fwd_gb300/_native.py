@@ -20,7 +20,8 @@ FA_ERR_WORKSPACE, FA_ERR_SCRATCH_LIMIT = -11, -12
 FA_DECODE_NOALLOC_SCRATCH_BYTES = 16 << 20  # fa.h: fixed scratch of fa_decode_noalloc, per device
 
 # Every symbol include/fa.h declares.
-EXPORTS = ("fa_forward", "fa_backward_dq", "fa_backward_dkdv", "fa_decode", "fa_decode_workspace_bytes",
+EXPORTS = ("fa_forward", "fa_backward_dq", "fa_backward_dkdv", "fa_backward_atomic", "fa_decode",
+           "fa_decode_workspace_bytes",
            "fa_decode_noalloc", "fa_status_string", "fa_device_status", "fa_selftest_timeout", "fa_selftest_exp2", "fa_version")
 
 _lib = None
@@ -41,6 +42,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_forward.argtypes = [_p, _p, _p, _p, _p, _i, _i, _i, _i, _f, _i, _i, _p]
     lib.fa_backward_dq.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _f, _i, _i, _i, _p]
     lib.fa_backward_dkdv.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _f, _i, _i, _i, _p]
+    lib.fa_backward_atomic.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, ctypes.c_size_t, _i, _i, _i, _i,
+                                       _f, _i, _i, _i, _p]
     lib.fa_decode.argtypes = [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _f, _i, _p, ctypes.c_size_t, _p]
     lib.fa_decode_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, ctypes.POINTER(ctypes.c_size_t)]
     lib.fa_decode_noalloc.argtypes = [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _f, _i, _p]
@@ -50,7 +53,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_selftest_timeout.argtypes = [_i, _p]
     lib.fa_selftest_exp2.argtypes = [_p, _p, _i, _p]
     lib.fa_version.argtypes = []
-    for name in ("fa_forward", "fa_backward_dq", "fa_backward_dkdv", "fa_decode", "fa_decode_workspace_bytes",
+    for name in ("fa_forward", "fa_backward_dq", "fa_backward_dkdv", "fa_backward_atomic", "fa_decode", "fa_decode_workspace_bytes",
                  "fa_decode_noalloc", "fa_device_status",
                  "fa_selftest_timeout", "fa_selftest_exp2", "fa_version"):
         getattr(lib, name).restype = _i

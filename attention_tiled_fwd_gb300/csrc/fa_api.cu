@@ -211,6 +211,33 @@ extern "C" int fa_backward_dkdv(const void *q, const void *k, const void *v, con
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+extern "C" int fa_backward_atomic(const void *q, const void *k, const void *v, const void *o, const void *dO,
+                                  const float *lse, float *delta, void *dq, void *dk, void *dv, float *dq_accum,
+                                  size_t dq_accum_bytes, int B, int H, int N, int D, float scale, int causal,
+                                  int dtype, int grad_dtype, void *stream) {
+    int rc = check_shape(B, H, N, D, scale);
+    if (rc != FA_OK) return rc;
+    if (dtype != FA_BF16 && dtype != FA_F32) return FA_ERR_DTYPE;
+    if (grad_dtype != FA_BF16 && grad_dtype != FA_F32) return FA_ERR_DTYPE;
+    if (dtype != FA_BF16) return FA_ERR_DTYPE;
+    if (D != 128) return FA_ERR_HEAD_DIM;
+    rc = check_ptrs({q, k, v, o, dO, lse, delta, dq, dk, dv, dq_accum});
+    if (rc != FA_OK) return rc;
+    if (dq_accum_bytes < (size_t)B * H * N * D * sizeof(float)) return FA_ERR_WORKSPACE;
+    int dev;
+    DeviceState *st;
+    rc = device_state(&dev, &st);
+    if (rc != FA_OK) return rc;
+    BwdArgs a{q, k, v, o, dO, lse, delta, dq_accum, dk, dv, B, H, N, D, scale, scale * log2e(),
+              causal ? 1 : 0, grad_dtype == FA_BF16 ? 1 : 0, st->status_word};
+    CUtensorMap tq, tk, tv, tdo;
+    if (encode_bf16_3d(&tq, q, B * H, N, D, kDkdvQRows) != FA_OK || encode_bf16_3d(&tk, k, B * H, N, D, 128) != FA_OK ||
+        encode_bf16_3d(&tv, v, B * H, N, D, 128) != FA_OK || encode_bf16_3d(&tdo, dO, B * H, N, D, kDkdvQRows) != FA_OK)
+        return FA_ERR_CUDA;
+    cudaError_t e = launch_bwd_atomic(a, dq, tq, tk, tv, tdo, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 namespace {
 int check_decode(int B, int H, int n_q, int N, int D, float scale) {
     int rc = check_shape(B, H, N, D, scale);

@@ -74,6 +74,11 @@ struct BwdArgs {
     int *status;
 };
 
+// 5-GEMM comparator backward (bwd_atomic.cu): a.dq is the fp32 accumulator
+// (B*H*N*D floats), dq_out the gradient in grad dtype; D = 128 only.
+cudaError_t launch_bwd_atomic(const BwdArgs &a, void *dq_out, const CUtensorMap &tq, const CUtensorMap &tk,
+                              const CUtensorMap &tv, const CUtensorMap &tdo, cudaStream_t s);
+
 // Decode (few query rows against a long key range), split over the keys.
 constexpr int kNumSms = 152;  // GB300
 

@@ -51,7 +51,9 @@ def step_flops(B, H, N, D, causal, passes=("fwd", "bwd")) -> float:
 def kernel_flops(B, H, N, D, causal):
     c = 0.5 if causal else 1.0
     u = B * H * float(N) * N * D * c
-    return {"fwd": 4 * u, "bwd_dq": 6 * u, "bwd_dkdv": 8 * u}
+    # the comparator backward is counted in the same 7-GEMM units as the split one (same work, same
+    # results), so the two lines compare directly; it performs 5 of those GEMMs
+    return {"fwd": 4 * u, "bwd_dq": 6 * u, "bwd_dkdv": 8 * u, "bwd_atomic": 14 * u}
 
 
 def aggregate(local_seconds: float, local_flops: float, world: int, reduce_max=None, reduce_sum=None):
@@ -315,6 +317,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--grad-dtype", choices=("bf16", "f32"), default="bf16")
+    ap.add_argument("--backward", choices=("split", "atomic"), default="split",
+                    help="split: fa_backward_dq + fa_backward_dkdv (the method); atomic: the 5-GEMM comparator "
+                         "fa_backward_atomic")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -376,14 +381,21 @@ def main():
         dk = torch.empty_like(dq)
         dv = torch.empty_like(dq)
         delta = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        dq_acc = torch.empty((B, H, N, D), dtype=torch.float32, device=dev) if args.backward == "atomic" else None
     stream = torch.cuda.current_stream()
-    kernels = ["fwd"] + (["bwd_dq", "bwd_dkdv"] if "bwd" in passes else [])
+    bwd_kernels = ["bwd_dq", "bwd_dkdv"] if args.backward == "split" else ["bwd_atomic"]
+    kernels = ["fwd"] + (bwd_kernels if "bwd" in passes else [])
 
     def step(evs=None):
         if evs:
             evs[0].record(stream)
         fa.fa_forward(q, k, v, scale=scale, causal=causal, o=o, lse=lse, stream=stream)
-        if "bwd" in passes:
+        if "bwd" in passes and args.backward == "atomic":
+            if evs:
+                evs[1].record(stream)
+            fa.fa_backward_atomic(q, k, v, o, dO, lse, scale=scale, causal=causal, dq_accum=dq_acc, dq=dq, dk=dk,
+                                  dv=dv, delta=delta, stream=stream)
+        elif "bwd" in passes:
             if evs:
                 evs[1].record(stream)
             fa.fa_backward_dq(q, k, v, o, dO, lse, scale=scale, causal=causal, dq=dq, delta=delta, stream=stream)
@@ -487,7 +499,8 @@ def main():
             "ms_per_step": 1e3 * t_max / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1), per-rank seed)",
             "config": {"workload": w.name, "B": B, "H": H, "N": N, "D": D, "causal": causal, "passes": list(passes),
-                       "grad_dtype": args.grad_dtype, "global_batch": B * world, "seq_len": N,
+                       "grad_dtype": args.grad_dtype, "backward": args.backward,
+                       "global_batch": B * world, "seq_len": N,
                        "parallelism": f"replicas x{world} (independent batches)",
                        "l2": "flushed before every timed step (512 MB write), outside the timed events"},
             "kernels": {kn: {"ms": mean_ms[kn], "tflops": kernel_tflops[kn],
@@ -495,7 +508,8 @@ def main():
             "roofline": roofline,
             "cpu_baseline": cpu_baseline,
             "e2e": e2e,
-            "gpu_launches": len(kernels) * args.steps,
+            # fa_backward_atomic launches three kernels (delta, the key-tile pass, dQ conversion)
+            "gpu_launches": (len(kernels) + (2 if args.backward == "atomic" and "bwd" in passes else 0)) * args.steps,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

@@ -113,6 +113,28 @@ FA_API int fa_backward_dkdv(const void *q, const void *k, const void *v, const v
                      int grad_dtype, void *stream);
 
 /*
+ * fa_backward_atomic -- the conventional 5-GEMM backward, as a comparator for
+ * the split backward above.  "FlashAttention (Metal port)" (metal-flash-
+ * attention), documentation section: the split into a dQ kernel and a dK/dV
+ * kernel (7 GEMMs, no atomics) is chosen there because Apple GPUs lack fp32
+ * atomics; this entry point runs the design that choice replaces.  One pass
+ * over key tiles recomputes S^T and dP^T once per (key tile, query tile),
+ * writes dK and dV, and accumulates dQ = dS K across key tiles in fp32 (one
+ * L2 bulk reduce-add per 64-query tile), then converts it:
+ *   delta = rowsum(dO * O)   (written, as fa_backward_dq writes it)
+ *   dq, dk, dv               (grad_dtype, same results as the split backward)
+ * dq_accum: device workspace owned by the caller, at least B*H*N*D*4 bytes,
+ * 16-byte aligned; zeroed and overwritten by the call (FA_ERR_WORKSPACE when
+ * smaller).  Supported: dtype FA_BF16, D = 128; grad_dtype FA_F32 or FA_BF16.
+ * Enqueues a memset and three kernels on `stream`.
+ */
+FA_API int fa_backward_atomic(const void *q, const void *k, const void *v, const void *o, const void *dO,
+                              const float *lse, float *delta, void *dq, void *dk, void *dv,
+                              float *dq_accum, size_t dq_accum_bytes,
+                              int B, int H, int N, int D, float scale, int causal, int dtype,
+                              int grad_dtype, void *stream);
+
+/*
  * fa_decode -- attention of a few query rows against a long key/value range
  * (decode).  "Flash Attention" (metalworking), section on the technique's
  * boundaries: one query row cannot fill a matrix-engine tile, so decode gets a
