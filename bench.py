@@ -449,38 +449,80 @@ def main():
                 "peak_source": f"{peak_kind} bf16_tflops (burst, cuBLAS bf16 GEMM)",
                 "peak_sustained": float(peaks.get("bf16_tflops_sustained", 0)) or None}
 
-    # ---- end to end through the public API: pinned host inputs in, results back out
+    # ---- end to end through the public API: pinned host inputs in, results back out.  Every step copies
+    # its inputs in and its gradients out; the copies of neighbouring steps overlap the step's kernels (H2D
+    # of step s+1 and D2H of step s-1 on their own streams, two buffer sets), as a training loop would.
     e2e = None
     if not args.no_e2e:
         pin = {n: t.pin_memory() for n, t in host.items()}
-        outs = {"o": torch.empty_like(o, device="cpu").pin_memory()}
-        if "bwd" in passes:
-            for n in ("dq", "dk", "dv"):
-                outs[n] = torch.empty((B, H, N, D), dtype=gdt).pin_memory()
+        out_names = ["o"] + (["dq", "dk", "dv"] if "bwd" in passes else [])
+        outs = [{n: torch.empty((B, H, N, D), dtype=(o.dtype if n == "o" else gdt)).pin_memory()
+                 for n in out_names} for _ in range(2)]
         h2d = sum(t.numel() * t.element_size() for t in pin.values())
-        d2h = sum(t.numel() * t.element_size() for t in outs.values())
+        d2h = sum(t.numel() * t.element_size() for t in outs[0].values())
+        # two device buffer sets: inputs, outputs and intermediates of one step each
+        bufs = []
+        for _ in range(2):
+            bset = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+            bset["o"] = torch.empty_like(o)
+            bset["lse"] = torch.empty_like(lse)
+            if "bwd" in passes:
+                for n in ("dq", "dk", "dv"):
+                    bset[n] = torch.empty((B, H, N, D), dtype=gdt, device=dev)
+                bset["delta"] = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+                if args.backward == "atomic":
+                    bset["acc"] = torch.empty((B, H, N, D), dtype=torch.float32, device=dev)
+            bufs.append(bset)
+
+        def run_step(bs, st):
+            fa.fa_forward(bs["q"], bs["k"], bs["v"], scale=scale, causal=causal, o=bs["o"], lse=bs["lse"], stream=st)
+            if "bwd" in passes and args.backward == "atomic":
+                fa.fa_backward_atomic(bs["q"], bs["k"], bs["v"], bs["o"], bs["dO"], bs["lse"], scale=scale,
+                                      causal=causal, dq_accum=bs["acc"], dq=bs["dq"], dk=bs["dk"], dv=bs["dv"],
+                                      delta=bs["delta"], stream=st)
+            elif "bwd" in passes:
+                fa.fa_backward_dq(bs["q"], bs["k"], bs["v"], bs["o"], bs["dO"], bs["lse"], scale=scale,
+                                  causal=causal, dq=bs["dq"], delta=bs["delta"], stream=st)
+                fa.fa_backward_dkdv(bs["q"], bs["k"], bs["v"], bs["dO"], bs["lse"], bs["delta"], scale=scale,
+                                    causal=causal, dk=bs["dk"], dv=bs["dv"], stream=st)
+
+        s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
         n_e2e = max(3, min(args.steps, 50))
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        in_done, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
         barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(n_e2e):
-            q.copy_(pin["q"], non_blocking=True)
-            k.copy_(pin["k"], non_blocking=True)
-            v.copy_(pin["v"], non_blocking=True)
-            if dO is not None:
-                dO.copy_(pin["dO"], non_blocking=True)
-            step()
-            outs["o"].copy_(o, non_blocking=True)
-            if "bwd" in passes:
-                outs["dq"].copy_(dq, non_blocking=True)
-                outs["dk"].copy_(dk, non_blocking=True)
-                outs["dv"].copy_(dv, non_blocking=True)
+        s_in.wait_event(e0)
+        s_out.wait_event(e0)
+        for it in range(n_e2e):
+            bi = it % 2
+            bs = bufs[bi]
+            with torch.cuda.stream(s_in):
+                if it >= 2:
+                    s_in.wait_event(comp_done[bi])  # step it-2 has finished reading this buffer set
+                for n, t in pin.items():
+                    bs[n].copy_(t, non_blocking=True)
+                in_done[bi].record(s_in)
+            stream.wait_event(in_done[bi])
+            if it >= 2:
+                stream.wait_event(out_done[bi])  # step it-2's results have been copied out
+            run_step(bs, stream)
+            comp_done[bi].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(comp_done[bi])
+                for n in out_names:
+                    outs[bi][n].copy_(bs[n], non_blocking=True)
+                out_done[bi].record(s_out)
+        stream.wait_event(out_done[(n_e2e - 1) % 2])
+        stream.wait_event(out_done[(n_e2e - 2) % 2])
         e1.record(stream)
         barrier()
         e2e_s = e0.elapsed_time(e1) / 1e3
         e2e_val, _ = aggregate(e2e_s, flops * n_e2e, world, reduce_max, reduce_sum)
         e2e = {"value": e2e_val / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "steps": n_e2e}
+               "steps": n_e2e,
+               "overlap": "H2D of step s+1 and D2H of step s-1 on their own streams while step s computes"}
 
     cpu_baseline = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
