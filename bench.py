@@ -259,7 +259,10 @@ def decode_main(args):
     import torch
     import attention_tiled_fwd_gb300 as fa
     dev = torch.device("cuda", 0)
-    B, H, nq, N, D = (DECODE_SHAPE[k] for k in ("B", "H", "n_q", "N", "D"))
+    shape = dict(DECODE_SHAPE)
+    if args.decode_shape:
+        shape.update(zip(("B", "H", "n_q", "N", "D"), (int(x) for x in args.decode_shape.split(","))))
+    B, H, nq, N, D = (shape[k] for k in ("B", "H", "n_q", "N", "D"))
     g = torch.Generator().manual_seed(2024)
     q = torch.randn(B, H, nq, D, generator=g).bfloat16().to(dev)
     k = torch.randn(B, H, N, D, generator=g).bfloat16().to(dev)
@@ -298,7 +301,7 @@ def decode_main(args):
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1))",
-            "config": {"workload": "decode", **DECODE_SHAPE, "causal": True,
+            "config": {"workload": "decode", **shape, "causal": True,
                        "l2": "flushed before every timed call (512 MB write), outside the timed events"},
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                          "traffic": None, "peak_source": f"{kind} hbm_gbs (copy)"},
@@ -317,6 +320,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--grad-dtype", choices=("bf16", "f32"), default="bf16")
+    ap.add_argument("--decode-shape", default="",
+                    help="B,H,n_q,N,D for --workload decode (default: the decode benchmark shape)")
     ap.add_argument("--backward", choices=("split", "atomic"), default="split",
                     help="split: fa_backward_dq + fa_backward_dkdv (the method); atomic: the 5-GEMM comparator "
                          "fa_backward_atomic")
