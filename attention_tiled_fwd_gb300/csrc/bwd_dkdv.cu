@@ -19,6 +19,10 @@
 // queries) of every tile's columns -- P^T and dS^T are elementwise given the
 // queries' L_i and D_i (broadcast from shared memory as float4), so the halves
 // never exchange data, and two warps per SM sub-partition hide latencies.
+// The producer warp also copies each query tile's L_i and D_i into a ring of
+// kStatSlots shared buffers (4-byte cp.async, zero fill past N, completion
+// tracked by the copies' own mbarrier arrivals), so no compute warp waits for
+// another to load or publish them.
 // TMEM (128 lanes = keys): S^T[b] = [64b, 64b+64), dP^T[b] = [128+64b, ...),
 // dV [256, 256+D), dK [256+D, 256+2D), b = i % 2.  The query tile is 64 rows so
 // that S^T and dP^T are double-buffered: the tensor core computes tile i+1
@@ -47,6 +51,7 @@ constexpr int kBQ = kDkdvQRows;   // queries per tile
 constexpr int kComputeWG = 2;     // compute warpgroups, one column half each
 constexpr int kFirstComputeWarp = 3;
 constexpr int kThreads = 32 * kFirstComputeWarp + 128 * kComputeWG;
+constexpr int kStatSlots = 4;     // query tiles' L / D in flight
 
 enum : int { kSiteKV = 41, kSiteSlotEmpty, kSiteSlotFull, kSiteSFull, kSitePReady, kSiteDpFull, kSiteDsReady,
              kSiteDone, kSiteFinal, kSiteDrain, kSiteStats, kSiteDvDone, kSiteDkDone };
@@ -58,11 +63,11 @@ struct DkdvSmem {
     static constexpr int kKOff = 0;
     static constexpr int kVOff = kKVBytes;
     static constexpr int kSlotOff = 2 * kKVBytes;
-    static constexpr int kStatOff = kSlotOff + NSLOT * kTileBytes;  // lse2[2][kBQ], delta[2][kBQ]
-    static constexpr int kBarOff = kStatOff + 4 * kBQ * 4;
+    static constexpr int kStatOff = kSlotOff + NSLOT * kTileBytes;  // [kStatSlots][L kBQ | D kBQ] fp32
+    static constexpr int kBarOff = kStatOff + kStatSlots * 2 * kBQ * 4;
     // kv_full, slot_full[NSLOT], slot_empty[NSLOT], s_full[2], dp_full[2], p_ready[2], ds_ready[2],
-    // stats[2], dv_done, dk_done, final, a_final
-    static constexpr int kNumBars = 1 + 2 * NSLOT + 14;
+    // stat_full[kStatSlots], stat_empty[kStatSlots], dv_done, dk_done, final, a_final
+    static constexpr int kNumBars = 1 + 2 * NSLOT + 8 + 2 * kStatSlots + 4;
     static constexpr int kTmemHolderOff = kBarOff + kNumBars * 8;
     static constexpr int kAlloc = kTmemHolderOff + 16 + 1024;
 };
@@ -83,8 +88,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *k_s = smem + L::kKOff;
     uint8_t *v_s = smem + L::kVOff;
     uint8_t *slots = smem + L::kSlotOff;
-    float *lse_s = reinterpret_cast<float *>(smem + L::kStatOff);  // [2][kBQ], already times log2(e)
-    float *del_s = lse_s + 2 * kBQ;                                 // [2][kBQ]
+    float *stat_s = reinterpret_cast<float *>(smem + L::kStatOff);  // slot s: L at [2 kBQ s], D after it
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
     uint64_t *kv_full = bars;
     uint64_t *slot_full = bars + 1;
@@ -93,8 +97,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *dp_full = s_full + 2;         // [2]
     uint64_t *p_ready = dp_full + 2;        // [2]
     uint64_t *ds_ready = p_ready + 2;       // [2]
-    uint64_t *stats_bar = ds_ready + 2;     // [2]: all compute threads are done with / published a stats buffer
-    uint64_t *dv_done = stats_bar + 2;
+    uint64_t *stat_full = ds_ready + 2;           // [kStatSlots]: a query tile's L / D landed
+    uint64_t *stat_empty = stat_full + kStatSlots;  // [kStatSlots]: every compute warp is done with it
+    uint64_t *dv_done = stat_empty + kStatSlots;
     uint64_t *dk_done = dv_done + 1;
     uint64_t *final_bar = dk_done + 1;   // issuer B: every dV / dK MMA has completed
     uint64_t *a_final = final_bar + 1;   // issuer A: every S^T / dP^T MMA has completed
@@ -120,7 +125,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&dp_full[b], 1);
             mbar_init(&p_ready[b], 4 * kComputeWG);  // one arrive per compute warp
             mbar_init(&ds_ready[b], 4 * kComputeWG);
-            mbar_init(&stats_bar[b], 4 * kComputeWG);
+        }
+        for (int t = 0; t < kStatSlots; ++t) {
+            mbar_init(&stat_full[t], 32);  // one arrival per producer lane, when its copies have landed
+            mbar_init(&stat_empty[t], 4 * kComputeWG);
         }
         mbar_init(dv_done, 1);
         mbar_init(dk_done, 1);
@@ -138,6 +146,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_holder;
 
     if (warp == 0) {
+        // TMA producer (lane 0): K, V once, then Q_i, dO_i into the ring.  The whole warp: each query
+        // tile's L_i, D_i into the stats ring (lanes 0-15 four L values each, lanes 16-31 four D values).
         if (lane == 0) {
             tma_prefetch_desc(&tmap_q);
             tma_prefetch_desc(&tmap_k);
@@ -149,28 +159,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_3d(k_s + p * (kBN * 128), &tmap_k, kv_full, p * 64, k_tile * kBN, bh);
                 tma_load_3d(v_s + p * (kBN * 128), &tmap_v, kv_full, p * 64, k_tile * kBN, bh);
             }
-            int last_round[NSLOT];
+        }
+        const float *lse_g = a.lse + (size_t)bh * N;
+        const float *del_g = a.delta + (size_t)bh * N;
+        int last_round[NSLOT];
 #pragma unroll
-            for (int s = 0; s < NSLOT; ++s) last_round[s] = -1;
-            for (int idx = 0; idx < 2 * n_q; ++idx) {
-                const int slot = idx % NSLOT, round = idx / NSLOT;
-                if (!mbar_wait(&slot_empty[slot], (round & 1) ^ 1, a.status, kSiteSlotEmpty)) break;
+        for (int s = 0; s < NSLOT; ++s) last_round[s] = -1;
+        bool ok = true;
+        for (int idx = 0; ok && idx < 2 * n_q; ++idx) {
+            const int slot = idx % NSLOT, round = idx / NSLOT;
+            if (!(ok = warp_wait(&slot_empty[slot], (round & 1) ^ 1, a.status, kSiteSlotEmpty))) break;
+            if (lane == 0) {
                 uint8_t *dst = slots + slot * L::kTileBytes;
                 const CUtensorMap *map = (idx & 1) ? &tmap_do : &tmap_q;
                 mbar_arrive_expect_tx(&slot_full[slot], L::kTileBytes);
 #pragma unroll
                 for (int p = 0; p < kPanels; ++p)
-                    tma_load_3d(dst + p * (kBQ * 128), map, &slot_full[slot], p * 64, (q_begin + (idx >> 1)) * kBQ,
-                                bh);
-#pragma unroll
-                for (int s = 0; s < NSLOT; ++s)
-                    if (s == slot) last_round[s] = round;
+                    tma_load_3d(dst + p * (kBQ * 128), map, &slot_full[slot], p * 64,
+                                (q_begin + (idx >> 1)) * kBQ, bh);
             }
+#pragma unroll
+            for (int s = 0; s < NSLOT; ++s)
+                if (s == slot) last_round[s] = round;
+            if (idx & 1) continue;
+            // stats of query tile i = idx / 2
+            const int i = idx >> 1, ss = i % kStatSlots, sr = i / kStatSlots;
+            if (!(ok = warp_wait(&stat_empty[ss], (sr & 1) ^ 1, a.status, kSiteStats))) break;
+            const bool is_l = lane < 16;
+            const int q = (q_begin + i) * kBQ + 4 * (lane & 15);
+            float *dst = stat_s + ss * 2 * kBQ + (is_l ? 0 : kBQ) + 4 * (lane & 15);
+            const float *src = is_l ? lse_g : del_g;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const bool valid = q + e < N;
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst + e)),
+                             "l"(src + (valid ? q + e : 0)), "r"(valid ? 4 : 0)
+                             : "memory");
+            }
+            asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&stat_full[ss]))
+                         : "memory");
+        }
+        // Drain: never leave the CTA with a copy still in flight.
+        if (lane == 0) {
 #pragma unroll
             for (int s = 0; s < NSLOT; ++s)
                 if (last_round[s] >= 0) mbar_wait(&slot_full[s], last_round[s] & 1, a.status, kSiteDrain);
             mbar_wait(kv_full, 0, a.status, kSiteDrain);
         }
+        asm volatile("cp.async.wait_all;" ::: "memory");
         __syncwarp();
     } else if (warp == 1) {
         // Issuer A: S^T_i = K Q_i^T and dP^T_i = V dO_i^T into buffer i % 2.  The whole warp runs the
@@ -264,39 +300,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int key = k_tile * kBN + r;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         const float c = a.scale_log2, sc = a.scale;
-        const float *lse_g = a.lse + (size_t)bh * N;
-        const float *del_g = a.delta + (size_t)bh * N;
         constexpr int kHalf = kBQ / kComputeWG;  // 32 queries per thread per tile
-        // threads 0..63 carry L (times log2 e) of query tid, threads 64..127 carry D of query tid - 64;
-        // every compute thread arrives on the stats barrier (so a buffer is rewritten only after all
-        // 256 threads finished reading it)
-        const bool carries = tid < 2 * kBQ;
-        const bool carries_lse = tid < kBQ;
-        const int stat_q = carries_lse ? tid : tid - kBQ;
-        auto load_stat = [&](int q_tile_idx) -> float {
-            if (!carries) return 0.f;
-            const int qi = q_tile_idx * kBQ + stat_q;
-            if (carries_lse) return qi < N ? lse_g[qi] * 1.4426950408889634f : INFINITY;
-            return qi < N ? del_g[qi] : 0.f;
-        };
-        auto store_stat = [&](int buf, float v) {
-            if (!carries) return;
-            if (carries_lse)
-                lse_s[buf * kBQ + stat_q] = v;
-            else
-                del_s[buf * kBQ + stat_q] = v;
-        };
         bool ok = true;
-        store_stat(0, load_stat(q_begin));
-        warp_arrive(&stats_bar[0]);
         for (int i = 0; i < n_q; ++i) {
             const int qt = q_begin + i;
             const int b = i & 1;
-            const float nxt = (i + 1 < n_q) ? load_stat(qt + 1) : 0.f;  // prefetch; published at the end
-            ok = mbar_wait(&stats_bar[b], (i >> 1) & 1, a.status, kSiteStats);
+            const int ss = i % kStatSlots;
+            ok = mbar_wait(&stat_full[ss], (i / kStatSlots) & 1, a.status, kSiteStats);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            const float4 *ls4 = reinterpret_cast<const float4 *>(lse_s + b * kBQ + g * kHalf);
-            const float4 *ds4 = reinterpret_cast<const float4 *>(del_s + b * kBQ + g * kHalf);
+            const float4 *ls4 = reinterpret_cast<const float4 *>(stat_s + ss * 2 * kBQ + g * kHalf);
+            const float4 *ds4 = reinterpret_cast<const float4 *>(stat_s + ss * 2 * kBQ + kBQ + g * kHalf);
             const int q0 = qt * kBQ + g * kHalf;  // first query of this thread's half
             // visible iff key <= query (causal), query < N and key < N
             const bool need_mask = (q0 + kHalf > N) || (a.causal && key > q0) || (key >= N);
@@ -313,12 +326,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_ld();
 #pragma unroll
                 for (int q4 = 0; q4 < kHalf / 4; ++q4) {
-                    const float4 l4 = ls4[q4];
+                    const float4 l4 = ls4[q4];  // natural-log L of four queries
+                    constexpr float kLog2e = 1.4426950408889634f;
                     float p[4];
-                    p[0] = ex2_approx(fmaf(__uint_as_float(raw[4 * q4 + 0]), c, -l4.x));
-                    p[1] = ex2_approx(fmaf(__uint_as_float(raw[4 * q4 + 1]), c, -l4.y));
-                    p[2] = ex2_approx(fmaf(__uint_as_float(raw[4 * q4 + 2]), c, -l4.z));
-                    p[3] = ex2_approx(fmaf(__uint_as_float(raw[4 * q4 + 3]), c, -l4.w));
+                    p[0] = ex2_approx(fmaf(__uint_as_float(raw[4 * q4 + 0]), c, -l4.x * kLog2e));
+                    p[1] = ex2_approx(fmaf(__uint_as_float(raw[4 * q4 + 1]), c, -l4.y * kLog2e));
+                    p[2] = ex2_approx(fmaf(__uint_as_float(raw[4 * q4 + 2]), c, -l4.z * kLog2e));
+                    p[3] = ex2_approx(fmaf(__uint_as_float(raw[4 * q4 + 3]), c, -l4.w * kLog2e));
                     if (any_mask) {
 #pragma unroll
                         for (int t = 0; t < 4; ++t) {
@@ -360,12 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_st();
             tc_fence_before();
             warp_arrive(&ds_ready[b]);
-            // Publish the next tile's stats into the other buffer.  Its readers (tile i-1) are done:
-            // every compute thread arrived on this tile's stats barrier only after finishing tile i-1.
-            if (i + 1 < n_q) {
-                store_stat(b ^ 1, nxt);
-                warp_arrive(&stats_bar[b ^ 1]);
-            }
+            warp_arrive(&stat_empty[ss]);  // this warp has read the tile's L and D
         }
         if (ok) {
             ok = mbar_wait(final_bar, 0, a.status, kSiteDone);
