@@ -20,16 +20,20 @@
 // L and D, so the halves never exchange data, and two warps per SM
 // sub-partition hide each other's latencies.
 // TMEM (128 lanes = queries): S[b] = [64b, 64b+64), dP[b] = [128+64b, ...),
-// dQ [256, 256+D), b = j % 2, and dS[j % 3] = [256+D+32(j%3), +32).  The key
-// tile is 64 rows so that S and dP are double-buffered: the tensor core
-// computes S_{j+1}, dP_{j+1} and dQ_{j-1} while the compute warps turn tile j
-// into dS.  Issue order after dS_j is ready: S_{j+2}, dP_{j+2}, then dQ_j.
-// dS (bf16) is the TMEM A operand of dQ += dS K_j; K_j is the B operand in
-// MN-major form (keys are the reduction).  tcgen05.mma operations on different
-// accumulators are not ordered with each other, so every buffer is rewritten
-// only after its previous reader is known complete: the compute warps write
-// dS_j after waiting for dQ_{j-3}, the previous reader of dS[j % 3] (three
-// buffers, so that wait is normally already satisfied); S_{j+2} / dP_{j+2}
+// dQ [256, 256+D), b = j % 2, dS[b] = [256+D+32b, +32), then Q (and, for
+// D = 64, dO) as bf16 pairs.  The key tile is 64 rows so that S and dP are
+// double-buffered: the tensor core computes S_{j+1}, dP_{j+1} and dQ_{j-1}
+// while the compute warps turn tile j into dS.  Q sits in TMEM so that
+// S = Q K_j^T runs as a TS MMA reading only K_j from shared memory: an N = 64
+// product with both operands in shared memory is bound by its bandwidth at two
+// thirds of the tensor rate.  (dO joins it at D = 64; at D = 128 the 512
+// columns are full.)  The compute warps copy Q (and dO) from the swizzled
+// shared tiles into TMEM once per CTA.  dS (bf16) is the TMEM A operand of
+// dQ += dS K_j; K_j is the B operand in MN-major form (keys are the
+// reduction).  tcgen05.mma operations on different accumulators are not
+// ordered with each other, so every buffer is rewritten only after its
+// previous reader is known complete: the compute warps write dS_j after
+// waiting for dQ_{j-2}, the previous reader of dS[j % 2]; S_{j+2} / dP_{j+2}
 // overwrite S[b] / dP[b] only after the compute warps finished tile j.  K_j is
 // released after dQ_j, which is issued only after S_j completed.
 #include "fa_internal.h"
@@ -46,7 +50,7 @@ constexpr int kFirstComputeWarp = 3;
 constexpr int kThreads = 32 * kFirstComputeWarp + 128 * kComputeWG;
 
 enum : int { kSiteQ = 21, kSiteSlotEmpty, kSiteSlotFull, kSiteSFull, kSiteDsFull, kSiteDq, kSiteFinal, kSiteDrain,
-             kSiteDqDone };
+             kSiteDqDone, kSiteQt };
 
 template <int D, int NSLOT>
 struct DqSmem {
@@ -56,7 +60,7 @@ struct DqSmem {
     static constexpr int kDoOff = kQBytes;
     static constexpr int kSlotOff = 2 * kQBytes;
     static constexpr int kBarOff = kSlotOff + NSLOT * kTileBytes;
-    // q_full, slot_full[NSLOT], slot_empty[NSLOT], s_full[2], ds_full[2], final, a_final, dq_done[3]
+    // q_full, slot_full[NSLOT], slot_empty[NSLOT], s_full[2], ds_full[2], final, a_final, dq_done[2], qt_ready
     static constexpr int kNumBars = 1 + 2 * NSLOT + 9;
     static constexpr int kTmemHolderOff = kBarOff + kNumBars * 8;
     static constexpr int kAlloc = kTmemHolderOff + 16 + 1024;
@@ -70,8 +74,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     using L = DqSmem<D, NSLOT>;
     constexpr int kPanels = D / 64;
     constexpr uint32_t kTmemCols = 512;
-    constexpr uint32_t kColDQ = 256, kColDS = 256 + D;
-    static_assert(kColDS + 96 <= 512, "TMEM budget");
+    constexpr bool kDoInTmem = D == 64;  // dO fits beside Q only at D = 64
+    constexpr uint32_t kColDQ = 256, kColDS = 256 + D, kColQ = kColDS + 64, kColDO = kColQ + D / 2;
+    static_assert(kColQ + (kDoInTmem ? D : D / 2) <= 512, "TMEM budget");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -86,7 +91,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *ds_full = s_full + 2;         // [2]: dS_j written (and S_j, dP_j read)
     uint64_t *final_bar = ds_full + 2;  // issuer B: every dQ MMA has completed
     uint64_t *a_final = final_bar + 1;  // issuer A: every S / dP MMA has completed
-    uint64_t *dq_done = a_final + 1;    // [3]: dQ_j completed (its dS buffer j % 3 is free)
+    uint64_t *dq_done = a_final + 1;    // [2]: dQ_j completed (its dS buffer j % 2 is free)
+    uint64_t *qt_ready = dq_done + 2;   // Q (and dO) are in TMEM
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kTmemHolderOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -109,7 +115,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(final_bar, 1);
         mbar_init(a_final, 1);
-        for (int b = 0; b < 3; ++b) mbar_init(&dq_done[b], 1);
+        for (int b = 0; b < 2; ++b) mbar_init(&dq_done[b], 1);
+        mbar_init(qt_ready, 4 * kComputeWG);  // one arrive per compute warp
         fence_mbarrier_init();
     }
     if (warp == 1) {
@@ -163,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t do_desc = sdesc_sw128(smem_u32(do_s), 16, 1024);
         const uint32_t slot_addr = smem_u32(slots);
         const bool leader = elect_one();
-        bool ok = warp_wait(q_full, 0, a.status, kSiteQ);
+        bool ok = warp_wait(q_full, 0, a.status, kSiteQ) && warp_wait(qt_ready, 0, a.status, kSiteQt);
         tc_fence_after();
         for (int j = 0; ok && j < n_kv; ++j) {
             const int k_slot = (2 * j) % NSLOT, k_round = (2 * j) / NSLOT;
@@ -179,12 +186,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (leader) {
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
-                    mma_ss(tmem + 64 * b, sdesc_add(q_desc, (ks >> 2) * (kBM * 128) + (ks & 3) * 32),
+                    mma_ts(tmem + 64 * b, tmem + kColQ + ks * 8,
                            sdesc_add(k_desc, (ks >> 2) * (kBN * 128) + (ks & 3) * 32), idesc_sq, ks > 0);
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks)
-                    mma_ss(tmem + 128 + 64 * b, sdesc_add(do_desc, (ks >> 2) * (kBM * 128) + (ks & 3) * 32),
-                           sdesc_add(v_desc, (ks >> 2) * (kBN * 128) + (ks & 3) * 32), idesc_sq, ks > 0);
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    if constexpr (kDoInTmem)
+                        mma_ts(tmem + 128 + 64 * b, tmem + kColDO + ks * 8,
+                               sdesc_add(v_desc, (ks >> 2) * (kBN * 128) + (ks & 3) * 32), idesc_sq, ks > 0);
+                    else
+                        mma_ss(tmem + 128 + 64 * b, sdesc_add(do_desc, (ks >> 2) * (kBM * 128) + (ks & 3) * 32),
+                               sdesc_add(v_desc, (ks >> 2) * (kBN * 128) + (ks & 3) * 32), idesc_sq, ks > 0);
+                }
                 mma_commit(&s_full[b]);
                 mma_commit(&slot_empty[v_slot]);  // V_j is no longer needed
             }
@@ -209,9 +221,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)
-                    mma_ts(tmem + kColDQ, tmem + kColDS + 32 * (j % 3) + kk * 8, sdesc_add(kmn_desc, kk * 2048),
+                    mma_ts(tmem + kColDQ, tmem + kColDS + 32 * b + kk * 8, sdesc_add(kmn_desc, kk * 2048),
                            idesc_dq, (j > 0 || kk > 0));
-                mma_commit(&dq_done[j % 3]);
+                mma_commit(&dq_done[b]);
                 mma_commit(&slot_empty[k_slot]);  // S_j completed before dS_j was produced
             }
             __syncwarp();
@@ -248,6 +260,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (g == 0) a.delta[(size_t)bh * N + row] = delta;
         }
+        // Q (and dO) rows into TMEM as bf16 pairs: warpgroup g copies the 64-column panels p with p % 2 == g
+        // (row r of a panel is 128 B at r * 128, its 16-byte chunk k stored at k ^ (r % 8))
+        {
+            bool qok = mbar_wait(q_full, 0, a.status, kSiteQ);
+            if (!__all_sync(0xffffffffu, qok)) qok = false;
+            if (qok) {
+#pragma unroll
+                for (int p = g; p < D / 64; p += 2) {
+#pragma unroll
+                    for (int m = 0; m < (kDoInTmem ? 2 : 1); ++m) {
+                        const uint8_t *panel = (m == 0 ? q_s : do_s) + p * (kBM * 128) + r * 128;
+                        uint32_t w[32];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const uint4 x = *reinterpret_cast<const uint4 *>(panel + ((k ^ (r & 7)) << 4));
+                            w[4 * k] = x.x;
+                            w[4 * k + 1] = x.y;
+                            w[4 * k + 2] = x.z;
+                            w[4 * k + 3] = x.w;
+                        }
+                        tmem_st32(tmem + lane_base + (m == 0 ? kColQ : kColDO) + 32 * p, w);
+                    }
+                }
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            warp_arrive(qt_ready);
+        }
         // P = 2^(S c - L log2 e); invalid rows get P = 0.
         const float lse2 = valid ? a.lse[(size_t)bh * N + row] * 1.4426950408889634f : INFINITY;
         const float sc = a.scale;
@@ -261,9 +301,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const int key0 = j * kBN + g * kHalf;
             const bool need_mask = (key0 + kHalf > N) || (a.causal && key0 + kHalf - 1 > q_tile * kBM);
-            // dS[j % 3] was last read by dQ_{j-3}
-            if (j >= 3) {
-                ok = mbar_wait(&dq_done[j % 3], ((j / 3) - 1) & 1, a.status, kSiteDqDone);
+            // dS[j % 2] was last read by dQ_{j-2}
+            if (j >= 2) {
+                ok = mbar_wait(&dq_done[b], ((j - 2) >> 1) & 1, a.status, kSiteDqDone);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc_fence_after();
             }
@@ -283,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float ds1 = p1 * (__uint_as_float(praw[i + 1]) - delta) * sc;
                 dsk[i / 2] = pack_bf16x2(ds0, ds1);
             }
-            tmem_st16(tmem + lane_base + kColDS + 32 * (j % 3) + g * (kHalf / 2), dsk);
+            tmem_st16(tmem + lane_base + kColDS + 32 * b + g * (kHalf / 2), dsk);
             tmem_wait_st();
             tc_fence_before();
             warp_arrive(&ds_full[b]);
