@@ -69,8 +69,8 @@ struct AtomicSmem {
     static constexpr int kStatOff = kDqOff + kBQ * D * 4;         // lse2[2][kBQ], delta[2][kBQ]
     static constexpr int kBarOff = kStatOff + 4 * kBQ * 4;
     // kv_full, slot_full[NSLOT], slot_empty[NSLOT], s_full[2], dp_full, p_ready[2], ds_ready, stats[2],
-    // dv_done, dk_done, dq_full, dq_free, tile_full, tile_free, final, a_final
-    static constexpr int kNumBars = 1 + 2 * NSLOT + 16;
+    // dv_done[2], dk_done, dq_full, dq_free, tile_full, tile_free, final, a_final
+    static constexpr int kNumBars = 1 + 2 * NSLOT + 17;
     static constexpr int kTmemHolderOff = kBarOff + kNumBars * 8;
     static constexpr int kAlloc = kTmemHolderOff + 16 + 1024;
 };
@@ -104,8 +104,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *p_ready = dp_full + 1;        // [2]
     uint64_t *ds_ready = p_ready + 2;       // dS^T(i) in TMEM and in shared memory
     uint64_t *stats_bar = ds_ready + 1;     // [2]
-    uint64_t *dv_done = stats_bar + 2;
-    uint64_t *dk_done = dv_done + 1;
+    // dV_i complete, one barrier per S^T buffer b = i % 2: issuer A waits for tile i - 2 while dV_{i-1}
+    // may already have completed, and on a single barrier that later phase would carry the parity it
+    // waits for.
+    uint64_t *dv_done = stats_bar + 2;      // [2]
+    uint64_t *dk_done = dv_done + 2;
     uint64_t *dq_full = dk_done + 1;        // dQ^T(i) complete (it has also read dS^T(i) from shared memory)
     uint64_t *dq_free = dq_full + 1;        // every compute warp has read dQ^T(i) out of TMEM
     uint64_t *tile_full = dq_free + 1;      // the staging tile holds dQ_i
@@ -136,7 +139,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(dp_full, 1);
         mbar_init(ds_ready, 4 * kComputeWG);
-        mbar_init(dv_done, 1);
+        mbar_init(&dv_done[0], 1);
+        mbar_init(&dv_done[1], 1);
         mbar_init(dk_done, 1);
         mbar_init(dq_full, 1);
         mbar_init(dq_free, 4 * kComputeWG);
@@ -205,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t b = i & 1;
             if (!(ok = warp_wait(&slot_full[q_slot], q_round & 1, a.status, kSiteSlotFull))) break;
             // S^T[b] last held P^T_{i-2}, read by dV_{i-2}
-            if (i >= 2 && !(ok = warp_wait(dv_done, (i - 2) & 1, a.status, kSiteDvDone))) break;
+            if (i >= 2 && !(ok = warp_wait(&dv_done[b], ((i - 2) >> 1) & 1, a.status, kSiteDvDone))) break;
             tc_fence_after();
             const uint64_t q_desc = sdesc_sw128(slot_addr + q_slot * L::kTileBytes, 16, 1024);
             if (leader) {
@@ -256,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < kBQ / 16; ++kk)
                     mma_ts(tmem + kColDV, tmem + 64 * b + (kk >> 1) * 32 + (kk & 1) * 8,
                            sdesc_add(dmn_desc, kk * 2048), idesc_g, (i > 0 || kk > 0));
-                mma_commit(dv_done);
+                mma_commit(&dv_done[b]);
             }
             __syncwarp();
             if (!(ok = warp_wait(ds_ready, i & 1, a.status, kSiteDsReady))) break;

@@ -232,6 +232,12 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
         : "memory");
 }
 
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t *r) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -242,6 +248,29 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r) {
         "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
         "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
+}
+
+// 32x32b loads / stores whose column count is a compile-time constant.
+template <int N>
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, uint32_t *r) {
+    static_assert(N == 16 || N == 32, "16 or 32 columns");
+    if constexpr (N == 32) {
+        tmem_ld32(taddr, r);
+    } else {
+        tmem_ld16(taddr, *reinterpret_cast<uint32_t(*)[16]>(r));
+    }
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_st_n(uint32_t taddr, const uint32_t *r) {
+    static_assert(N == 8 || N == 16 || N == 32, "8, 16 or 32 columns");
+    if constexpr (N == 32) {
+        tmem_st32(taddr, r);
+    } else if constexpr (N == 16) {
+        tmem_st16(taddr, r);
+    } else {
+        tmem_st8(taddr, r);
+    }
 }
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
