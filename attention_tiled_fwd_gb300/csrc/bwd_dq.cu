@@ -18,7 +18,11 @@
 // two warpgroups, each thread owning one query row (its TMEM lane) and one
 // half (32 keys) of every tile's columns -- dS is elementwise given the row's
 // L and D, so the halves never exchange data, and two warps per SM
-// sub-partition hide each other's latencies.
+// sub-partition hide each other's latencies (four warpgroups of 16 keys
+// measured 3 % slower here).  The compute warps compute D while Q and dO are
+// loading, each warpgroup over its own share of the row: D over the whole row
+// per thread outlasted the load and delayed the first products, by ~12 % of
+// the kernel's time at N = 4096; D after the Q copy delayed the first dS.
 // TMEM (128 lanes = queries): S[b] = [64b, 64b+64), dP[b] = [128+64b, ...),
 // dQ [256, 256+D), b = j % 2, dS[b] = [256+D+32b, +32), then Q (and, for
 // D = 64, dO) as bf16 pairs.  The key tile is 64 rows so that S and dP are
@@ -45,7 +49,7 @@ namespace {
 
 constexpr int kBM = 128;          // queries per CTA (TMEM lanes)
 constexpr int kBN = kDqKRows;     // keys per tile
-constexpr int kComputeWG = 2;     // compute warpgroups, one column half each
+constexpr int kComputeWG = 2;     // compute warpgroups, one 32-key half of every tile each
 constexpr int kFirstComputeWarp = 3;
 constexpr int kThreads = 32 * kFirstComputeWarp + 128 * kComputeWG;
 
@@ -59,7 +63,8 @@ struct DqSmem {
     static constexpr int kQOff = 0;
     static constexpr int kDoOff = kQBytes;
     static constexpr int kSlotOff = 2 * kQBytes;
-    static constexpr int kBarOff = kSlotOff + NSLOT * kTileBytes;
+    static constexpr int kDeltaOff = kSlotOff + NSLOT * kTileBytes;  // [kComputeWG][kBM] partial sums of dO * O
+    static constexpr int kBarOff = kDeltaOff + kComputeWG * kBM * 4;
     // q_full, slot_full[NSLOT], slot_empty[NSLOT], s_full[2], ds_full[2], final, a_final, dq_done[2], qt_ready
     static constexpr int kNumBars = 1 + 2 * NSLOT + 9;
     static constexpr int kTmemHolderOff = kBarOff + kNumBars * 8;
@@ -83,6 +88,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *q_s = smem + L::kQOff;
     uint8_t *do_s = smem + L::kDoOff;
     uint8_t *slots = smem + L::kSlotOff;
+    float *delta_s = reinterpret_cast<float *>(smem + L::kDeltaOff);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
     uint64_t *q_full = bars;
     uint64_t *slot_full = bars + 1;
@@ -233,21 +239,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         warp_wait(final_bar, 0, a.status, kSiteFinal);
     } else {
         const int quarter = warp & 3;
-        const int g = (warp - kFirstComputeWarp) >> 2;  // column half of every tile
+        const int g = (warp - kFirstComputeWarp) >> 2;  // key range of every tile
         const int r = quarter * 32 + lane;
         const int row = q_tile * kBM + r;
         const bool valid = row < N;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         const float c = a.scale_log2;
-        // D_i = sum_d dO_id O_id for this thread's row (both halves compute it; half 0 stores it).
+        // P = 2^(S c - L log2 e); invalid rows get P = 0.
+        const float lse2 = valid ? a.lse[(size_t)bh * N + row] * 1.4426950408889634f : INFINITY;
+        // D_i = sum_d dO_id O_id for this thread's row, while the producer's TMA brings in Q and dO (nothing
+        // can start before they land): warpgroup g sums columns [g D / kComputeWG, (g + 1) D / kComputeWG),
+        // the partial sums meet in shared memory, and every warpgroup adds them in the same order.
+        constexpr int kDCols = D / kComputeWG;
         float delta = 0.f;
         if (valid) {
             const uint4 *orow = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.o) +
-                                                                ((size_t)bh * N + row) * D);
+                                                                ((size_t)bh * N + row) * D + g * kDCols);
             const uint4 *drow = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.dO) +
-                                                                ((size_t)bh * N + row) * D);
+                                                                ((size_t)bh * N + row) * D + g * kDCols);
 #pragma unroll 4
-            for (int i = 0; i < D / 8; ++i) {
+            for (int i = 0; i < kDCols / 8; ++i) {
                 const uint4 ov = orow[i], dv = drow[i];
                 const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, dw[4] = {dv.x, dv.y, dv.z, dv.w};
 #pragma unroll
@@ -258,18 +269,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     delta = fmaf(of.y, df.y, delta);
                 }
             }
-            if (g == 0) a.delta[(size_t)bh * N + row] = delta;
         }
-        // Q (and dO) rows into TMEM as bf16 pairs: warpgroup g copies the 64-column panels p with p % 2 == g
+        delta_s[g * kBM + r] = delta;
+        // every compute warp reaches this barrier: nothing before it waits or exits early
+        asm volatile("bar.sync 1, %0;" ::"r"(128 * kComputeWG) : "memory");
+        delta = 0.f;
+#pragma unroll
+        for (int t = 0; t < kComputeWG; ++t) delta += delta_s[t * kBM + r];
+        if (valid && g == 0) a.delta[(size_t)bh * N + row] = delta;
+        const float sc = a.scale;
+        const int lim = a.causal ? min(N - 1, row) : N - 1;  // last visible key
+        // Q (and dO) rows into TMEM as bf16 pairs, one 64-column panel per warpgroup in turn
         // (row r of a panel is 128 B at r * 128, its 16-byte chunk k stored at k ^ (r % 8))
         {
             bool qok = mbar_wait(q_full, 0, a.status, kSiteQ);
             if (!__all_sync(0xffffffffu, qok)) qok = false;
             if (qok) {
+                constexpr int kItems = (kDoInTmem ? 2 : 1) * kPanels;  // (matrix, panel) pairs
 #pragma unroll
-                for (int p = g; p < D / 64; p += 2) {
-#pragma unroll
-                    for (int m = 0; m < (kDoInTmem ? 2 : 1); ++m) {
+                for (int t = g; t < kItems; t += kComputeWG) {
+                    const int m = t / kPanels, p = t % kPanels;
+                    {
                         const uint8_t *panel = (m == 0 ? q_s : do_s) + p * (kBM * 128) + r * 128;
                         uint32_t w[32];
 #pragma unroll
@@ -288,11 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             warp_arrive(qt_ready);
         }
-        // P = 2^(S c - L log2 e); invalid rows get P = 0.
-        const float lse2 = valid ? a.lse[(size_t)bh * N + row] * 1.4426950408889634f : INFINITY;
-        const float sc = a.scale;
-        const int lim = a.causal ? min(N - 1, row) : N - 1;  // last visible key
-        constexpr int kHalf = kBN / kComputeWG;              // 32 columns per thread per tile
+        constexpr int kHalf = kBN / kComputeWG;              // columns per thread per tile
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
             const uint32_t b = j & 1;
@@ -308,8 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
             }
             uint32_t sraw[kHalf], praw[kHalf], dsk[kHalf / 2];
-            tmem_ld32(tmem + lane_base + 64 * b + g * kHalf, sraw);
-            tmem_ld32(tmem + lane_base + 128 + 64 * b + g * kHalf, praw);
+            tmem_ld_n<kHalf>(tmem + lane_base + 64 * b + g * kHalf, sraw);
+            tmem_ld_n<kHalf>(tmem + lane_base + 128 + 64 * b + g * kHalf, praw);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < kHalf; i += 2) {
@@ -323,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float ds1 = p1 * (__uint_as_float(praw[i + 1]) - delta) * sc;
                 dsk[i / 2] = pack_bf16x2(ds0, ds1);
             }
-            tmem_st16(tmem + lane_base + kColDS + 32 * b + g * (kHalf / 2), dsk);
+            tmem_st_n<kHalf / 2>(tmem + lane_base + kColDS + 32 * b + g * (kHalf / 2), dsk);
             tmem_wait_st();
             tc_fence_before();
             warp_arrive(&ds_full[b]);
@@ -334,18 +350,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok) {
             tc_fence_after();
-            uint32_t v[32];
+            constexpr int kCols = D / kComputeWG;  // this warpgroup's columns of dQ
+            constexpr int kChunk = kCols < 32 ? kCols : 32;
+            uint32_t v[kChunk];
 #pragma unroll
-            for (int ch = 0; ch < D / 64; ++ch) {  // this half's D/2 columns of dQ
-                const int col = g * (D / 2) + ch * 32;
-                tmem_ld32(tmem + lane_base + kColDQ + col, v);
+            for (int ch = 0; ch < kCols / kChunk; ++ch) {
+                const int col = g * kCols + ch * kChunk;
+                tmem_ld_n<kChunk>(tmem + lane_base + kColDQ + col, v);
                 tmem_wait_ld();
                 if (valid) {
                     if (a.grad_bf16) {
                         uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.dq) +
                                                                ((size_t)bh * N + row) * D + col);
 #pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4) {
+                        for (int v4 = 0; v4 < kChunk / 8; ++v4) {
                             uint4 w;
                             w.x = pack_bf16x2(__uint_as_float(v[v4 * 8 + 0]), __uint_as_float(v[v4 * 8 + 1]));
                             w.y = pack_bf16x2(__uint_as_float(v[v4 * 8 + 2]), __uint_as_float(v[v4 * 8 + 3]));
@@ -357,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.dq) +
                                                                  ((size_t)bh * N + row) * D + col);
 #pragma unroll
-                        for (int v4 = 0; v4 < 8; ++v4)
+                        for (int v4 = 0; v4 < kChunk / 4; ++v4)
                             dst[v4] = make_float4(__uint_as_float(v[v4 * 4 + 0]), __uint_as_float(v[v4 * 4 + 1]),
                                                   __uint_as_float(v[v4 * 4 + 2]), __uint_as_float(v[v4 * 4 + 3]));
                     }
