@@ -39,8 +39,7 @@ constexpr int kDkdvQRows = 64;  // dK/dV kernel: 128 keys per CTA, 64-query Q/dO
 // longest tiles and fills the tail with short ones.  Non-causal tiles are
 // equal, so the tiles of one head stay adjacent (they share its K/V in L2).
 #ifdef __CUDACC__
-__device__ __forceinline__ void tile_order(int n_tiles, int n_bh, bool causal, int *rank, int *bh) {
-    const int L = blockIdx.x;
+__device__ __forceinline__ void tile_order_at(int L, int n_tiles, int n_bh, bool causal, int *rank, int *bh) {
     if (causal) {
         *rank = L / n_bh;
         *bh = L % n_bh;
@@ -48,6 +47,10 @@ __device__ __forceinline__ void tile_order(int n_tiles, int n_bh, bool causal, i
         *rank = L % n_tiles;
         *bh = L / n_tiles;
     }
+}
+
+__device__ __forceinline__ void tile_order(int n_tiles, int n_bh, bool causal, int *rank, int *bh) {
+    tile_order_at(blockIdx.x, n_tiles, n_bh, causal, rank, bh);
 }
 #endif
 
