@@ -52,6 +52,15 @@ __device__ __forceinline__ void tile_order_at(int L, int n_tiles, int n_bh, bool
 __device__ __forceinline__ void tile_order(int n_tiles, int n_bh, bool causal, int *rank, int *bh) {
     tile_order_at(blockIdx.x, n_tiles, n_bh, causal, rank, bh);
 }
+
+// The k-th work item of CTA c in a persistent grid of G CTAs (one per SM): round k of the 1-D work
+// order above is dealt out forwards in even rounds and backwards in odd ones, so a CTA that drew a heavy
+// item in one round draws a light one in the next.  -1: no item for this CTA in round k.
+__device__ __forceinline__ int persistent_work_index(int k, int n_work) {
+    const int G = gridDim.x, c = blockIdx.x;
+    const int Lw = k * G + ((k & 1) ? G - 1 - c : c);
+    return Lw < n_work ? Lw : -1;
+}
 #endif
 
 struct FwdArgs {

@@ -27,7 +27,7 @@
 // S_X(j+1) is issued after pv_done_X(j), which also orders the softmax's O
 // rescale of step j+1 after PV_X(j); the epilogue reads O_X after the block's
 // last pv_done_X, and the next block's first PV_X waits until it has (o_free).
-// Persistent grid: one CTA per SM walks a sequence of blocks (pair_work_index),
+// Persistent grid: one CTA per SM walks a sequence of blocks (persistent_work_index),
 // so a block's Q load and first S products overlap the previous block's last
 // products and epilogue instead of a CTA exit, launch and pipeline fill
 // (measured +10 % at B=2 H=16 N=4096 D=128 causal, +5 % at N=32768 D=64).
@@ -83,15 +83,6 @@ __device__ __forceinline__ PairBlock pair_block(const FwdArgs &a, int L, int n_b
     w.n_all = max(w.n_kv0, w.n_kv1);  // >= 1
     w.n_q_tiles = (w.row0 + kBM < a.N) ? kTiles : 1;  // a query tile wholly past N is not loaded
     return w;
-}
-
-// The k-th block of CTA c in a persistent grid of G CTAs: round k of the 1-D work order (heaviest first
-// for causal launches) is dealt out forwards in even rounds and backwards in odd ones, so a CTA that drew
-// a heavy block in one round draws a light one in the next (-1: no block for this CTA in round k).
-__device__ __forceinline__ int pair_work_index(int k, int n_work) {
-    const int G = gridDim.x, c = blockIdx.x;
-    const int Lw = k * G + ((k & 1) ? G - 1 - c : c);
-    return Lw < n_work ? Lw : -1;
 }
 
 // Persistent: the grid has at most one CTA per SM, each walking its blocks in turn, so the next block's
@@ -167,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int nb = 0;    // blocks so far
             bool ok = true;
             for (int k = 0; ok && k * (int)gridDim.x < n_work; ++k) {
-                const int Lw = pair_work_index(k, n_work);
+                const int Lw = persistent_work_index(k, n_work);
                 if (Lw < 0) continue;
                 const PairBlock w = pair_block(a, Lw, n_blk);
                 // Q of this block goes after its first K and V tiles: its buffer frees only when the
@@ -223,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int blocks[kTiles] = {0, 0};  // earlier blocks in which tile x had work (epilogues)
         int nb = 0;
         for (int k = 0; ok && k * (int)gridDim.x < n_work; ++k) {
-            const int Lw = pair_work_index(k, n_work);
+            const int Lw = persistent_work_index(k, n_work);
             if (Lw < 0) continue;
             const PairBlock w = pair_block(a, Lw, n_blk);
             const int n_kv[kTiles] = {w.n_kv0, w.n_kv1};
@@ -314,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         int step0 = 0;  // steps of this tile before the current block
         for (int k = 0; ok && k * (int)gridDim.x < n_work; ++k) {
-            const int Lw = pair_work_index(k, n_work);
+            const int Lw = persistent_work_index(k, n_work);
             if (Lw < 0) continue;
             const PairBlock w = pair_block(a, Lw, n_blk);
             const int n = x == 0 ? w.n_kv0 : w.n_kv1;
