@@ -4,9 +4,11 @@
 //
 //   per query tile i:  S^T = K Q_i^T,  P^T = exp(S^T scale - L_i) (base 2 here),
 //                      dV += P^T dO_i,
-//                      dP^T = V dO_i^T,  dS^T = P^T * (dP^T - D_i) * scale,
+//                      dP^T = V dO_i^T,  dS^T = P^T * (dP^T - D_i),
 //                      dK += dS^T Q_i
-//   dK, dV written once after the last query tile.  Four GEMMs per tile, no
+//   dK (times the softmax scale, which every dS^T carries and which is
+//   applied once here instead of per score) and dV written once after the
+//   last query tile.  Four GEMMs per tile, no
 //   atomics, no scratch.  Causal: only query tiles on or below the diagonal
 //   (queries >= keys) are visited.
 //
@@ -331,21 +333,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = mbar_wait(&s_full[b], (i >> 1) & 1, a.status, kSiteSFull);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
-            // P^T row half as bf16 pairs: the dV operand, and (unpacked) the factor of dS^T below.
+            // P^T of this thread's queries: bf16 pairs for the dV operand, fp32 pairs kept for dS^T below.
+            // The arithmetic runs on fp32 pairs (f32x2), two scores per instruction.
             uint32_t pk[kHalf / 2];
+            uint64_t p2[kHalf / 2];
             {
                 uint32_t raw[kHalf];
                 tmem_ld_n<kHalf>(tmem + lane_base + 64 * b + g * kHalf, raw);
                 tmem_wait_ld();
+                constexpr float kLog2e = 1.4426950408889634f;
+                const uint64_t c2 = f2_pack(c, c), nlog2e2 = f2_pack(-kLog2e, -kLog2e);
 #pragma unroll
                 for (int q4 = 0; q4 < kHalf / 4; ++q4) {
                     const float4 l4 = ls4[q4];  // natural-log L of four queries
-                    constexpr float kLog2e = 1.4426950408889634f;
                     float p[4];
-                    p[0] = ex2_approx(fmaf(__uint_as_float(raw[4 * q4 + 0]), c, -l4.x * kLog2e));
-                    p[1] = ex2_approx(fmaf(__uint_as_float(raw[4 * q4 + 1]), c, -l4.y * kLog2e));
-                    p[2] = ex2_approx(fmaf(__uint_as_float(raw[4 * q4 + 2]), c, -l4.z * kLog2e));
-                    p[3] = ex2_approx(fmaf(__uint_as_float(raw[4 * q4 + 3]), c, -l4.w * kLog2e));
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(raw[4 * q4 + 0]), __uint_as_float(raw[4 * q4 + 1])), c2,
+                                     f2_mul(f2_pack(l4.x, l4.y), nlog2e2)),
+                              p[0], p[1]);
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(raw[4 * q4 + 2]), __uint_as_float(raw[4 * q4 + 3])), c2,
+                                     f2_mul(f2_pack(l4.z, l4.w), nlog2e2)),
+                              p[2], p[3]);
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) p[t] = ex2_approx(p[t]);
                     if (any_mask) {
 #pragma unroll
                         for (int t = 0; t < 4; ++t) {
@@ -353,6 +362,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (qq >= N || key >= N || (a.causal && qq < key)) p[t] = 0.f;
                         }
                     }
+                    p2[2 * q4] = f2_pack(p[0], p[1]);
+                    p2[2 * q4 + 1] = f2_pack(p[2], p[3]);
                     pk[2 * q4] = pack_bf16x2(p[0], p[1]);
                     pk[2 * q4 + 1] = pack_bf16x2(p[2], p[3]);
                 }
@@ -372,15 +383,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int q4 = 0; q4 < kHalf / 4; ++q4) {
                     const float4 d4 = ds4[q4];
-                    const float2 p01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&pk[2 * q4]));
-                    const float2 p23 =
-                        __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&pk[2 * q4 + 1]));
-                    const float d0 = p01.x * (__uint_as_float(raw[4 * q4 + 0]) - d4.x) * sc;
-                    const float d1 = p01.y * (__uint_as_float(raw[4 * q4 + 1]) - d4.y) * sc;
-                    const float d2 = p23.x * (__uint_as_float(raw[4 * q4 + 2]) - d4.z) * sc;
-                    const float d3 = p23.y * (__uint_as_float(raw[4 * q4 + 3]) - d4.w) * sc;
-                    dsk[2 * q4] = pack_bf16x2(d0, d1);
-                    dsk[2 * q4 + 1] = pack_bf16x2(d2, d3);
+                    // dS^T / scale = P^T * (dP^T - D), on fp32 pairs
+                    dsk[2 * q4] = f2_to_bf16x2(f2_mul(
+                        f2_sub(f2_pack(__uint_as_float(raw[4 * q4 + 0]), __uint_as_float(raw[4 * q4 + 1])),
+                               f2_pack(d4.x, d4.y)),
+                        p2[2 * q4]));
+                    dsk[2 * q4 + 1] = f2_to_bf16x2(f2_mul(
+                        f2_sub(f2_pack(__uint_as_float(raw[4 * q4 + 2]), __uint_as_float(raw[4 * q4 + 3])),
+                               f2_pack(d4.z, d4.w)),
+                        p2[2 * q4 + 1]));
                 }
                 tmem_st_n<kHalf / 2>(tmem + lane_base + 128 + 64 * b + g * kHalf, dsk);
             }
@@ -402,12 +413,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int c0 = (g % (kComputeWG / 2)) * kCols;
             const uint32_t col = (is_dv ? kColDV : kColDK) + c0;
             void *outp = is_dv ? a.dv : a.dk;
+            const float osc = is_dv ? 1.f : sc;  // dK picks up the scale its dS^T operands left out
             uint32_t v[32];
 #pragma unroll
             for (int ch = 0; ch < kCols / 32; ++ch) {
                 tmem_ld32(tmem + lane_base + col + ch * 32, v);
                 tmem_wait_ld();
                 if (!valid) continue;
+#pragma unroll
+                for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * osc);
                 if (a.grad_bf16) {
                     uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(outp) +
                                                            ((size_t)bh * N + key) * D + c0 + ch * 32);

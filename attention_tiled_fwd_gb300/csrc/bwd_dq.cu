@@ -4,9 +4,10 @@
 //
 //   D_i = sum_d dO_id O_id                          (prologue, written out)
 //   per K/V tile j:  S = Q K_j^T,  P = exp(S scale - L)  (base 2 here),
-//                    dP = dO V_j^T,  dS = P * (dP - D) * scale,
+//                    dP = dO V_j^T,  dS = P * (dP - D),
 //                    dQ += dS K_j
-//   dQ written once after the last tile.  Three GEMMs per tile; no atomics and
+//   dQ written once after the last tile, times the softmax scale (which every
+//   dS carries; applied once here instead of per score).  Three GEMMs per tile; no atomics and
 //   no scratch: each CTA owns its dQ rows outright (the design the page adopts
 //   because float atomics are emulated on its GPU; it parallelises fully over
 //   query rows here as there).
@@ -277,7 +278,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int t = 0; t < kComputeWG; ++t) delta += delta_s[t * kBM + r];
         if (valid && g == 0) a.delta[(size_t)bh * N + row] = delta;
-        const float sc = a.scale;
         const int lim = a.causal ? min(N - 1, row) : N - 1;  // last visible key
         // Q (and dO) rows into TMEM as bf16 pairs, one 64-column panel per warpgroup in turn
         // (row r of a panel is 128 B at r * 128, its 16-byte chunk k stored at k ^ (r % 8))
@@ -309,6 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             warp_arrive(qt_ready);
         }
         constexpr int kHalf = kBN / kComputeWG;              // columns per thread per tile
+        const uint64_t c2 = f2_pack(c, c), nl2 = f2_pack(-lse2, -lse2), d2 = f2_pack(delta, delta);
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
             const uint32_t b = j & 1;
@@ -327,17 +328,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld_n<kHalf>(tmem + lane_base + 64 * b + g * kHalf, sraw);
             tmem_ld_n<kHalf>(tmem + lane_base + 128 + 64 * b + g * kHalf, praw);
             tmem_wait_ld();
+            // dS / scale = P * (dP - D), on fp32 pairs (f32x2), two scores per instruction
 #pragma unroll
             for (int i = 0; i < kHalf; i += 2) {
-                float p0 = ex2_approx(fmaf(__uint_as_float(sraw[i]), c, -lse2));
-                float p1 = ex2_approx(fmaf(__uint_as_float(sraw[i + 1]), c, -lse2));
+                float p0, p1;
+                f2_unpack(f2_fma(f2_pack(__uint_as_float(sraw[i]), __uint_as_float(sraw[i + 1])), c2, nl2), p0, p1);
+                p0 = ex2_approx(p0);
+                p1 = ex2_approx(p1);
                 if (need_mask) {
                     if (key0 + i > lim) p0 = 0.f;
                     if (key0 + i + 1 > lim) p1 = 0.f;
                 }
-                const float ds0 = p0 * (__uint_as_float(praw[i]) - delta) * sc;
-                const float ds1 = p1 * (__uint_as_float(praw[i + 1]) - delta) * sc;
-                dsk[i / 2] = pack_bf16x2(ds0, ds1);
+                dsk[i / 2] = f2_to_bf16x2(
+                    f2_mul(f2_sub(f2_pack(__uint_as_float(praw[i]), __uint_as_float(praw[i + 1])), d2), f2_pack(p0, p1)));
             }
             tmem_st_n<kHalf / 2>(tmem + lane_base + kColDS + 32 * b + g * (kHalf / 2), dsk);
             tmem_wait_st();
@@ -358,6 +361,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int col = g * kCols + ch * kChunk;
                 tmem_ld_n<kChunk>(tmem + lane_base + kColDQ + col, v);
                 tmem_wait_ld();
+#pragma unroll
+                for (int t = 0; t < kChunk; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * a.scale);
                 if (valid) {
                     if (a.grad_bf16) {
                         uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.dq) +
