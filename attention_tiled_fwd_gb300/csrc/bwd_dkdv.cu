@@ -22,7 +22,9 @@
 // queries' L_i and D_i (broadcast from shared memory as float4), so the
 // quarters never exchange data, and four compute warps per SM sub-partition
 // hide the latencies of the TMEM loads and the exponentials (measured 2.6 %
-// faster at D = 128 and 6 % at D = 64 than two warpgroups of 32 queries).
+// faster at D = 128 than two warpgroups of 32 queries).  This kernel serves
+// D = 128; D = 64 runs bwd_dkdv_q128.cu, whose 128-query tiles make S^T and
+// dP^T N = 128 products.
 // The producer warp also copies each query tile's L_i and D_i into a ring of
 // kStatSlots shared buffers (4-byte cp.async, zero fill past N, completion
 // tracked by the copies' own mbarrier arrivals), so no compute warp waits for
@@ -472,7 +474,6 @@ cudaError_t launch_spec(const BwdArgs &a, const CUtensorMap &tq, const CUtensorM
 cudaError_t launch_bwd_dkdv(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             const CUtensorMap &tdo, cudaStream_t s) {
     switch (a.D) {
-        case 64: return launch_spec<64, 16>(a, tq, tk, tv, tdo, s);
         case 128: return launch_spec<128, 8>(a, tq, tk, tv, tdo, s);
         default: return cudaErrorInvalidValue;
     }

@@ -25,15 +25,16 @@
 // per thread outlasted the load and delayed the first products, by ~12 % of
 // the kernel's time at N = 4096; D after the Q copy delayed the first dS.
 // TMEM (128 lanes = queries): S[b] = [64b, 64b+64), dP[b] = [128+64b, ...),
-// dQ [256, 256+D), b = j % 2, dS[b] = [256+D+32b, +32), then Q (and, for
-// D = 64, dO) as bf16 pairs.  The key tile is 64 rows so that S and dP are
-// double-buffered: the tensor core computes S_{j+1}, dP_{j+1} and dQ_{j-1}
-// while the compute warps turn tile j into dS.  Q sits in TMEM so that
+// dQ [256, 256+D), b = j % 2, dS[b] = [256+D+32b, +32), then Q as bf16
+// pairs.  This kernel serves D = 128 (D = 64 runs bwd_dq_k128.cu, whose
+// 128-key tiles make S and dP N = 128 products).  The key tile is 64 rows so
+// that S and dP are double-buffered: the tensor core computes S_{j+1},
+// dP_{j+1} and dQ_{j-1} while the compute warps turn tile j into dS.  Q sits in TMEM so that
 // S = Q K_j^T runs as a TS MMA reading only K_j from shared memory: an N = 64
 // product with both operands in shared memory is bound by its bandwidth at two
-// thirds of the tensor rate.  (dO joins it at D = 64; at D = 128 the 512
-// columns are full.)  The compute warps copy Q (and dO) from the swizzled
-// shared tiles into TMEM once per CTA.  dS (bf16) is the TMEM A operand of
+// thirds of the tensor rate.  (dO has no room beside it: the 512 columns are
+// full, so dP reads both operands from shared memory.)  The compute warps copy
+// Q from the swizzled shared tiles into TMEM once per CTA.  dS (bf16) is the TMEM A operand of
 // dQ += dS K_j; K_j is the B operand in MN-major form (keys are the
 // reduction).  tcgen05.mma operations on different accumulators are not
 // ordered with each other, so every buffer is rewritten only after its
@@ -80,9 +81,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     using L = DqSmem<D, NSLOT>;
     constexpr int kPanels = D / 64;
     constexpr uint32_t kTmemCols = 512;
-    constexpr bool kDoInTmem = D == 64;  // dO fits beside Q only at D = 64
-    constexpr uint32_t kColDQ = 256, kColDS = 256 + D, kColQ = kColDS + 64, kColDO = kColQ + D / 2;
-    static_assert(kColQ + (kDoInTmem ? D : D / 2) <= 512, "TMEM budget");
+    constexpr uint32_t kColDQ = 256, kColDS = 256 + D, kColQ = kColDS + 64;
+    static_assert(kColQ + D / 2 <= 512, "TMEM budget");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *final_bar = ds_full + 2;  // issuer B: every dQ MMA has completed
     uint64_t *a_final = final_bar + 1;  // issuer A: every S / dP MMA has completed
     uint64_t *dq_done = a_final + 1;    // [2]: dQ_j completed (its dS buffer j % 2 is free)
-    uint64_t *qt_ready = dq_done + 2;   // Q (and dO) are in TMEM
+    uint64_t *qt_ready = dq_done + 2;   // Q is in TMEM
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kTmemHolderOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -196,14 +196,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_ts(tmem + 64 * b, tmem + kColQ + ks * 8,
                            sdesc_add(k_desc, (ks >> 2) * (kBN * 128) + (ks & 3) * 32), idesc_sq, ks > 0);
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    if constexpr (kDoInTmem)
-                        mma_ts(tmem + 128 + 64 * b, tmem + kColDO + ks * 8,
-                               sdesc_add(v_desc, (ks >> 2) * (kBN * 128) + (ks & 3) * 32), idesc_sq, ks > 0);
-                    else
-                        mma_ss(tmem + 128 + 64 * b, sdesc_add(do_desc, (ks >> 2) * (kBM * 128) + (ks & 3) * 32),
-                               sdesc_add(v_desc, (ks >> 2) * (kBN * 128) + (ks & 3) * 32), idesc_sq, ks > 0);
-                }
+                for (int ks = 0; ks < D / 16; ++ks)
+                    mma_ss(tmem + 128 + 64 * b, sdesc_add(do_desc, (ks >> 2) * (kBM * 128) + (ks & 3) * 32),
+                           sdesc_add(v_desc, (ks >> 2) * (kBN * 128) + (ks & 3) * 32), idesc_sq, ks > 0);
                 mma_commit(&s_full[b]);
                 mma_commit(&slot_empty[v_slot]);  // V_j is no longer needed
             }
@@ -279,29 +274,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < kComputeWG; ++t) delta += delta_s[t * kBM + r];
         if (valid && g == 0) a.delta[(size_t)bh * N + row] = delta;
         const int lim = a.causal ? min(N - 1, row) : N - 1;  // last visible key
-        // Q (and dO) rows into TMEM as bf16 pairs, one 64-column panel per warpgroup in turn
+        // Q rows into TMEM as bf16 pairs, one 64-column panel per warpgroup
         // (row r of a panel is 128 B at r * 128, its 16-byte chunk k stored at k ^ (r % 8))
         {
             bool qok = mbar_wait(q_full, 0, a.status, kSiteQ);
             if (!__all_sync(0xffffffffu, qok)) qok = false;
             if (qok) {
-                constexpr int kItems = (kDoInTmem ? 2 : 1) * kPanels;  // (matrix, panel) pairs
 #pragma unroll
-                for (int t = g; t < kItems; t += kComputeWG) {
-                    const int m = t / kPanels, p = t % kPanels;
-                    {
-                        const uint8_t *panel = (m == 0 ? q_s : do_s) + p * (kBM * 128) + r * 128;
-                        uint32_t w[32];
+                for (int p = g; p < kPanels; p += kComputeWG) {
+                    const uint8_t *panel = q_s + p * (kBM * 128) + r * 128;
+                    uint32_t w[32];
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            const uint4 x = *reinterpret_cast<const uint4 *>(panel + ((k ^ (r & 7)) << 4));
-                            w[4 * k] = x.x;
-                            w[4 * k + 1] = x.y;
-                            w[4 * k + 2] = x.z;
-                            w[4 * k + 3] = x.w;
-                        }
-                        tmem_st32(tmem + lane_base + (m == 0 ? kColQ : kColDO) + 32 * p, w);
+                    for (int k = 0; k < 8; ++k) {
+                        const uint4 x = *reinterpret_cast<const uint4 *>(panel + ((k ^ (r & 7)) << 4));
+                        w[4 * k] = x.x;
+                        w[4 * k + 1] = x.y;
+                        w[4 * k + 2] = x.z;
+                        w[4 * k + 3] = x.w;
                     }
+                    tmem_st32(tmem + lane_base + kColQ + 32 * p, w);
                 }
                 tmem_wait_st();
             }
@@ -415,7 +406,6 @@ cudaError_t launch_spec(const BwdArgs &a, const CUtensorMap &tq, const CUtensorM
 cudaError_t launch_bwd_dq(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                           const CUtensorMap &tdo, cudaStream_t s) {
     switch (a.D) {
-        case 64: return launch_spec<64, 16>(a, tq, tk, tv, tdo, s);
         case 128: return launch_spec<128, 8>(a, tq, tk, tv, tdo, s);
         default: return cudaErrorInvalidValue;
     }
