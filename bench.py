@@ -102,19 +102,93 @@ def traffic_for(kernel: str, workload: str):
     return e["bytes_per_launch"] if e.get("source_hash") == cur else None
 
 
+# NVML clock-event reason bits (nvml.h, nvmlClocksEventReason*) that the timing rules name.
+NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+                0x80: "hw_power_brake_slowdown"}
+
+
+def decode_reasons(mask: int):
+    """Names of the clock-event reasons set in an NVML reason bit mask."""
+    return sorted(name for bit, name in NVML_REASONS.items() if mask & bit)
+
+
+class NvmlReader:
+    """Read-only NVML queries through ctypes: SM clock, its maximum, power draw and the clock-event
+    reasons of one GPU, found by PCI bus id (so CUDA and NVML agree on the device).  Nothing is set."""
+
+    def __init__(self, lib, handle, reasons_fn):
+        self.lib, self.h, self.reasons_fn = lib, handle, reasons_fn
+
+    @classmethod
+    def open(cls, pci_domain: int, pci_bus: int, pci_device: int):
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return None
+            h = ctypes.c_void_p()
+            bus = f"{pci_domain:08x}:{pci_bus:02x}:{pci_device:02x}.0".encode()
+            if lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) != 0:
+                return None
+            reasons_fn = None
+            for name in ("nvmlDeviceGetCurrentClocksEventReasons", "nvmlDeviceGetCurrentClocksThrottleReasons"):
+                try:
+                    reasons_fn = getattr(lib, name)
+                    break
+                except AttributeError:
+                    continue
+            if reasons_fn is None:
+                return None
+            r = cls(lib, h, reasons_fn)
+            return r if r.read() is not None else None
+        except (OSError, AttributeError):
+            return None
+
+    def read(self):
+        import ctypes
+        sm, mx, mw = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint()
+        reasons = ctypes.c_ulonglong()
+        NVML_CLOCK_SM = 1
+        if (self.lib.nvmlDeviceGetClockInfo(self.h, NVML_CLOCK_SM, ctypes.byref(sm)) != 0 or
+                self.lib.nvmlDeviceGetMaxClockInfo(self.h, NVML_CLOCK_SM, ctypes.byref(mx)) != 0 or
+                self.reasons_fn(self.h, ctypes.byref(reasons)) != 0):
+            return None
+        power = mw.value / 1000.0 if self.lib.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(mw)) == 0 else None
+        return {"sm_mhz": float(sm.value), "sm_max_mhz": float(mx.value), "power_w": power,
+                "reasons": int(reasons.value)}
+
+
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 100 ms while running."""
+    """SM clocks and clock-event reasons sampled while the timed region runs: through NVML every 2 ms
+    when it can be opened (reader: an object with read() -> dict as NvmlReader gives), else through
+    nvidia-smi every 50 ms."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, reader=None, period_s: float = 0.002):
         self.gpu = gpu_index
+        self.reader = reader
+        self.period = period_s
         self.proc = None
-        self.lines = []
+        self.running = False
+        self.lines = []    # nvidia-smi: (time, csv line)
+        self.samples = []  # NVML: (time, dict)
         self.t_start = self.t_stop = None
 
     def start(self):
+        if self.reader is None:
+            try:
+                import torch
+                p = torch.cuda.get_device_properties(self.gpu)
+                self.reader = NvmlReader.open(p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+            except Exception:
+                self.reader = None
+        if self.reader is not None:
+            self.running = True
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "50"],
@@ -124,6 +198,13 @@ class ClockSampler:
             return
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
+
+    def _poll(self):
+        while self.running:
+            r = self.reader.read()
+            if r is not None:
+                self.samples.append((time.time(), r))
+            time.sleep(self.period)
 
     def _read(self):
         for line in self.proc.stdout:
@@ -135,7 +216,24 @@ class ClockSampler:
     def mark_stop(self):
         self.t_stop = time.time()
 
+    def _inside(self, t):
+        return self.t_start is not None and self.t_start <= t <= (self.t_stop or 1e30)
+
     def stop(self):
+        if self.reader is not None and self.running:
+            self.running = False
+            self.thread.join(timeout=1.0)
+            inside = [r for t, r in self.samples if self._inside(t)]
+            used = inside if inside else [r for _, r in self.samples[-2:]]
+            mhz = [r["sm_mhz"] for r in used]
+            mask = 0
+            for r in used:
+                mask |= r["reasons"]
+            power = [r["power_w"] for r in used if r["power_w"] is not None]
+            return {"sm_mhz": statistics.median(mhz) if mhz else None,
+                    "sm_max_mhz": max(r["sm_max_mhz"] for r in used) if used else None,
+                    "reasons": decode_reasons(mask), "samples": len(inside),
+                    "power_w_max": max(power) if power else None, "source": "nvml, every 2 ms"}
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         time.sleep(0.15)
@@ -150,7 +248,7 @@ class ClockSampler:
             if len(parts) < 9:
                 continue
             rows.append((t, parts))
-        inside = [r for r in rows if self.t_start is not None and self.t_start <= r[0] <= (self.t_stop or 1e30)]
+        inside = [r for r in rows if self._inside(r[0])]
         used = inside if inside else rows[-2:]
         mhz = [float(p[1]) for _, p in used if p[1].replace(".", "").isdigit()]
         mx = [float(p[2]) for _, p in used if p[2].replace(".", "").isdigit()]
@@ -159,7 +257,7 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": max(mx) if mx else None,
                 "reasons": reasons, "samples": len(inside),
                 "power_w_max": max((float(p[3]) for _, p in used if p[3].replace(".", "").isdigit()),
-                                   default=None)}
+                                   default=None), "source": "nvidia-smi, every 50 ms"}
 
 
 # ----------------------------------------------------------------------------- CPU baseline (the oracle)
