@@ -25,6 +25,7 @@ struct DeviceState {
     bool ready = false;
     int status_code = 0;  // FA_OK or the fa_status of the failed set-up
     int *status_word = nullptr;
+    int num_sms = kNumSms;  // the device's SM count (sizes persistent grids)
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -48,6 +49,7 @@ int device_state(int *dev_out, DeviceState **st_out) {
     if (!st.ready) {
         cudaDeviceProp prop;
         if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return FA_ERR_CUDA;
+        st.num_sms = prop.multiProcessorCount > 0 ? prop.multiProcessorCount : kNumSms;
         if (!(prop.major == 10 && prop.minor == 3)) {
             st.status_code = FA_ERR_DEVICE;  // kernels are built for sm_103a only
         } else if (cudaGetSymbolAddress(reinterpret_cast<void **>(&st.status_word), g_status_word) != cudaSuccess) {
@@ -142,7 +144,7 @@ extern "C" int fa_forward(const void *q, const void *k, const void *v, void *o, 
     rc = device_state(&dev, &st);
     if (rc != FA_OK) return rc;
 
-    FwdArgs a{q, k, v, o, lse, B, H, N, D, scale, scale * log2e(), causal ? 1 : 0, st->status_word};
+    FwdArgs a{q, k, v, o, lse, B, H, N, D, scale, scale * log2e(), causal ? 1 : 0, st->status_word, st->num_sms};
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (dtype == FA_F32) {

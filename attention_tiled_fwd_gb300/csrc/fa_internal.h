@@ -72,6 +72,7 @@ struct FwdArgs {
     float scale_log2;  // scale * log2(e): scores go straight to the base-2 domain
     int causal;
     int *status;       // device status word (bounded-wait failures)
+    int num_sms;       // SMs of the device: the persistent forward runs one CTA per SM
 };
 
 struct BwdArgs {

@@ -438,7 +438,8 @@ cudaError_t launch_spec(const FwdArgs &a, const CUtensorMap &tq, const CUtensorM
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     const int n_work = ((a.N + kTiles * kBM - 1) / (kTiles * kBM)) * a.H * a.B;
-    dim3 grid(n_work < kNumSms ? n_work : kNumSms);
+    const int sms = a.num_sms > 0 ? a.num_sms : kNumSms;
+    dim3 grid(n_work < sms ? n_work : sms);
     kern<<<grid, kThreads, L::kAlloc, s>>>(tq, tk, tv, a);
     return cudaGetLastError();
 }
