@@ -11,6 +11,13 @@ Metric: attention TFLOP/s with the FLOPs counted algorithmically -- forward
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--no-e2e] [--no-cpu-baseline]
+                    [--no-workloads] [--sustained-s S]
+
+Besides the headline step, the JSON line carries (at N=1) a ``workloads``
+object with every workload shape of the path (each fp32 / bf16 forward, both
+masks where both are run, the forward + backward cases), each timed the same
+way with its own clock record, and a ``sustained`` object: the headline step
+repeated back to back for several seconds, against the sustained tensor peak.
 
 Timing: CUDA events on the launching stream around each kernel of each step;
 L2 is flushed (a 512 MB write) before every timed step, outside the events;
@@ -56,6 +63,23 @@ def kernel_flops(B, H, N, D, causal):
     return {"fwd": 4 * u, "bwd_dq": 6 * u, "bwd_dkdv": 8 * u, "bwd_atomic": 14 * u}
 
 
+def backward_flops(B, H, N, D, causal):
+    """The backward's FLOPs under both conventions: the 7 GEMMs the split backward runs (14 B H N^2 D)
+    and the conventional 5-GEMM count (10 B H N^2 D), both halved for causal."""
+    c = 0.5 if causal else 1.0
+    u = B * H * float(N) * N * D * c
+    return {"7gemm": 14 * u, "5gemm": 10 * u}
+
+
+def backward_summary(ms_dq: float, ms_dkdv: float, B, H, N, D, causal, peak: float) -> dict:
+    """The split backward (dQ kernel + dK/dV kernel) as one number under both FLOP conventions."""
+    ms = ms_dq + ms_dkdv
+    f = backward_flops(B, H, N, D, causal)
+    t7 = f["7gemm"] / (ms * 1e-3) / 1e12
+    t5 = f["5gemm"] / (ms * 1e-3) / 1e12
+    return {"ms": ms, "tflops_7gemm": t7, "frac_7gemm": t7 / peak, "tflops_5gemm": t5, "frac_5gemm": t5 / peak}
+
+
 def aggregate(local_seconds: float, local_flops: float, world: int, reduce_max=None, reduce_sum=None):
     """Whole-job throughput: all ranks' FLOPs over the slowest rank's time."""
     t = reduce_max(local_seconds) if reduce_max else local_seconds
@@ -80,15 +104,24 @@ def source_hash(paths) -> str:
     return h.hexdigest()[:16]
 
 
-KERNEL_SOURCES = {
-    "fwd": ["attention_tiled_fwd_gb300/csrc/fwd_bf16.cu", "attention_tiled_fwd_gb300/csrc/fwd_bf16_pair.cu",
-            "attention_tiled_fwd_gb300/csrc/sm100_ptx.cuh"],
-    "bwd_dq": ["attention_tiled_fwd_gb300/csrc/bwd_dq.cu", "attention_tiled_fwd_gb300/csrc/sm100_ptx.cuh"],
-    "bwd_dkdv": ["attention_tiled_fwd_gb300/csrc/bwd_dkdv.cu", "attention_tiled_fwd_gb300/csrc/sm100_ptx.cuh"],
-}
+CSRC = "attention_tiled_fwd_gb300/csrc/"
 
 
-def traffic_for(kernel: str, workload: str):
+def kernel_sources(kernel: str, D: int, dtype: str = "bf16"):
+    """The source files whose kernels run for `kernel` at head dimension D (for keying ncu figures)."""
+    common = [CSRC + "sm100_ptx.cuh", CSRC + "fa_internal.h"]
+    if kernel == "fwd":
+        if dtype == "f32":
+            return [CSRC + "fwd_f32.cu", CSRC + "fa_internal.h"]
+        return [CSRC + "fwd_bf16.cu", CSRC + "fwd_bf16_pair.cu"] + common
+    if kernel == "bwd_dq":
+        return [CSRC + ("bwd_dq_k128.cu" if D == 64 else "bwd_dq.cu")] + common
+    if kernel == "bwd_dkdv":
+        return [CSRC + ("bwd_dkdv_q128.cu" if D == 64 else "bwd_dkdv.cu")] + common
+    return [CSRC + "bwd_atomic.cu"] + common
+
+
+def traffic_for(kernel: str, workload: str, D: int = 128, dtype: str = "bf16"):
     """DRAM bytes per launch from the committed ncu summary, if taken on the current source."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(p):
@@ -98,7 +131,7 @@ def traffic_for(kernel: str, workload: str):
     e = d.get(workload, {}).get(kernel)
     if not e:
         return None
-    cur = source_hash([os.path.join(ROOT, s) for s in KERNEL_SOURCES[kernel]])
+    cur = source_hash([os.path.join(ROOT, s) for s in kernel_sources(kernel, D, dtype)])
     return e["bytes_per_launch"] if e.get("source_hash") == cur else None
 
 
@@ -407,6 +440,144 @@ def decode_main(args):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------- every workload, one GPU
+def workload_keys():
+    """(key, workload, causal) for every workload shape and mask the path is run in."""
+    from synthetic_inputs import WORKLOADS
+    out = []
+    for w in WORKLOADS.values():
+        for causal in w.causal:
+            key = w.name if len(w.causal) == 1 else f"{w.name}_{'causal' if causal else 'noncausal'}"
+            out.append((key, w, causal))
+    return out
+
+
+def time_workload(fa, torch, dev, w, causal, steps: int, warmup: int, flush, peaks) -> dict:
+    """One workload timed like the headline step: the forward (and, where the workload has one, the
+    split backward with bf16 gradients) per step, CUDA events around every kernel on the launching
+    stream, L2 flushed before every step outside the events, SM clocks sampled during the K steps."""
+    from synthetic_inputs import make_qkv
+    B, H, N, D = w.B, w.H, w.N, w.D
+    bwd = "bwd" in w.passes
+    host = make_qkv(B, H, N, D, w.seed, w.dtype, w.std, with_dO=bwd)
+    q, k, v = (host[n].to(dev) for n in ("q", "k", "v"))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    kernels = ["fwd"]
+    if bwd:
+        dO = host["dO"].to(dev)
+        dq, dk, dv = (torch.empty((B, H, N, D), dtype=torch.bfloat16, device=dev) for _ in range(3))
+        delta = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        kernels += ["bwd_dq", "bwd_dkdv"]
+    stream = torch.cuda.current_stream()
+    scale = w.scale
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        fa.fa_forward(q, k, v, scale=scale, causal=causal, o=o, lse=lse, stream=stream)
+        if bwd:
+            if evs:
+                evs[1].record(stream)
+            fa.fa_backward_dq(q, k, v, o, dO, lse, scale=scale, causal=causal, dq=dq, delta=delta, stream=stream)
+            if evs:
+                evs[2].record(stream)
+            fa.fa_backward_dkdv(q, k, v, dO, lse, delta, scale=scale, causal=causal, dk=dk, dv=dv, stream=stream)
+        if evs:
+            evs[-1].record(stream)
+
+    for _ in range(warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(kernels) + 1)] for _ in range(steps)]
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    time.sleep(0.1)
+    torch.cuda.synchronize()
+    sampler.mark_start()
+    for it in range(steps):
+        flush.fill_(float(it))
+        step(events[it])
+    torch.cuda.synchronize()
+    sampler.mark_stop()
+    clocks = sampler.stop()
+    if fa.fa_device_status() != 0:
+        raise RuntimeError(f"device status reports a failure in workload {w.name}")
+    ms = {kn: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in events) for i, kn in enumerate(kernels)}
+    step_ms = statistics.mean(e[0].elapsed_time(e[-1]) for e in events)
+    kf = kernel_flops(B, H, N, D, causal)
+    peak = float(peaks["bf16_tflops"])
+    entry = {"B": B, "H": H, "N": N, "D": D, "causal": causal, "dtype": w.dtype, "steps": steps,
+             "warmup": warmup, "gpu_launches": len(kernels) * steps, "clocks": clocks}
+    if w.dtype == "f32":
+        # the fp32 FFMA forward: a parity path without a tensor-core roofline; its time is the figure
+        entry["kernels"] = {"fwd": {"us": 1e3 * ms["fwd"], "tflops": kf["fwd"] / (ms["fwd"] * 1e-3) / 1e12,
+                                    "traffic": traffic_for("fwd", w.name, D, "f32")}}
+        entry["step_ms"] = step_ms
+        return entry
+    key_traffic = w.name if len(w.causal) == 1 else f"{w.name}_{'causal' if causal else 'noncausal'}"
+    entry["kernels"] = {kn: {"ms": ms[kn], "tflops": kf[kn] / (ms[kn] * 1e-3) / 1e12,
+                             "frac_of_peak": kf[kn] / (ms[kn] * 1e-3) / 1e12 / peak,
+                             "traffic": traffic_for(kn, key_traffic, D)} for kn in kernels}
+    if bwd:
+        entry["backward"] = backward_summary(ms["bwd_dq"], ms["bwd_dkdv"], B, H, N, D, causal, peak)
+    f = step_flops(B, H, N, D, causal, w.passes)
+    entry["step_ms"] = step_ms
+    entry["step_tflops"] = f / (step_ms * 1e-3) / 1e12
+    entry["step_frac_of_peak"] = entry["step_tflops"] / peak
+    return entry
+
+
+def time_sustained(fa, torch, dev, w, seconds: float, step_ms_hint: float, peaks) -> dict:
+    """The headline step repeated back to back for `seconds`, timed as one region by two CUDA events,
+    with clocks and power sampled throughout: the figure to hold against the sustained tensor peak.
+    No L2 flush between steps: one step's tensors (Q, K, V, O, dO, dQ, dK, dV) exceed the L2."""
+    from synthetic_inputs import make_qkv
+    B, H, N, D = w.B, w.H, w.N, w.D
+    causal = w.causal[0]
+    host = make_qkv(B, H, N, D, w.seed, w.dtype, w.std, with_dO=True)
+    q, k, v, dO = (host[n].to(dev) for n in ("q", "k", "v", "dO"))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty((B, H, N, D), dtype=torch.bfloat16, device=dev) for _ in range(3))
+    delta = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        fa.fa_forward(q, k, v, scale=w.scale, causal=causal, o=o, lse=lse, stream=stream)
+        fa.fa_backward_dq(q, k, v, o, dO, lse, scale=w.scale, causal=causal, dq=dq, delta=delta, stream=stream)
+        fa.fa_backward_dkdv(q, k, v, dO, lse, delta, scale=w.scale, causal=causal, dk=dk, dv=dv, stream=stream)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    n = int(min(50000, max(10, math.ceil(seconds * 1e3 / max(step_ms_hint, 1e-3)))))
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    time.sleep(0.1)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    sampler.mark_start()
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark_stop()
+    clocks = sampler.stop()
+    if fa.fa_device_status() != 0:
+        raise RuntimeError("device status reports a failure in the sustained run")
+    total_s = e0.elapsed_time(e1) / 1e3
+    tflops = step_flops(B, H, N, D, causal, ("fwd", "bwd")) * n / total_s / 1e12
+    sus = float(peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"])
+    return {"workload": w.name, "steps": n, "seconds": total_s, "ms_per_step": 1e3 * total_s / n,
+            "tflops": tflops, "peak_sustained": sus, "frac_of_sustained_peak": tflops / sus,
+            "frac_of_burst_peak": tflops / float(peaks["bf16_tflops"]), "gpu_launches": 3 * n,
+            "l2": "not flushed: one step's tensors (268 MB at this shape) exceed the 129 MB L2",
+            "clocks": clocks}
+
+
 # ----------------------------------------------------------------------------- GPU arm
 def main():
     ap = argparse.ArgumentParser()
@@ -417,6 +588,11 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the per-workload timings (every workload shape, each with its own clocks)")
+    ap.add_argument("--workload-steps", type=int, default=10, help="timed steps per workload in `workloads`")
+    ap.add_argument("--sustained-s", type=float, default=3.0,
+                    help="seconds of back-to-back headline steps for `sustained` (0: skip)")
     ap.add_argument("--grad-dtype", choices=("bf16", "f32"), default="bf16")
     ap.add_argument("--decode-shape", default="",
                     help="B,H,n_q,N,D for --workload decode (default: the decode benchmark shape)")
@@ -548,9 +724,23 @@ def main():
     peaks, peak_kind = load_peaks()
     peak = float(peaks["bf16_tflops"])
     roofline = {"bound": "tensor", "kernel": dom, "achieved": kernel_tflops[dom], "peak": peak,
-                "unit": "TFLOP/s", "frac": kernel_tflops[dom] / peak, "traffic": traffic_for(dom, w.name),
+                "unit": "TFLOP/s", "frac": kernel_tflops[dom] / peak, "traffic": traffic_for(dom, w.name, D),
                 "peak_source": f"{peak_kind} bf16_tflops (burst, cuBLAS bf16 GEMM)",
                 "peak_sustained": float(peaks.get("bf16_tflops_sustained", 0)) or None}
+
+    backward = (backward_summary(mean_ms["bwd_dq"], mean_ms["bwd_dkdv"], B, H, N, D, causal, peak)
+                if "bwd_dq" in mean_ms else None)
+
+    # ---- every workload shape, then the headline step held for several seconds (one GPU only)
+    workloads = sustained = None
+    if world == 1 and not args.no_workloads:
+        workloads = {}
+        for key, ww, cz in workload_keys():
+            workloads[key] = time_workload(fa, torch, dev, ww, cz, max(3, args.workload_steps), 3, flush, peaks)
+            torch.cuda.empty_cache()
+    if world == 1 and args.sustained_s > 0 and "bwd" in passes and args.backward == "split":
+        sustained = time_sustained(fa, torch, dev, w, args.sustained_s, 1e3 * t_max / args.steps, peaks)
+        torch.cuda.empty_cache()
 
     # ---- end to end through the public API: pinned host inputs in, results back out.  Every step copies
     # its inputs in and its gradients out; the copies of neighbouring steps overlap the step's kernels (H2D
@@ -650,12 +840,15 @@ def main():
                        "l2": "flushed before every timed step (512 MB write), outside the timed events"},
             "kernels": {kn: {"ms": mean_ms[kn], "tflops": kernel_tflops[kn],
                              "frac_of_peak": kernel_tflops[kn] / peak} for kn in kernels},
+            "backward": backward,
             "roofline": roofline,
             "cpu_baseline": cpu_baseline,
             "e2e": e2e,
             # fa_backward_atomic launches three kernels (delta, the key-tile pass, dQ conversion)
             "gpu_launches": (len(kernels) + (2 if args.backward == "atomic" and "bwd" in passes else 0)) * args.steps,
             "clocks": clocks,
+            "workloads": workloads,
+            "sustained": sustained,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
