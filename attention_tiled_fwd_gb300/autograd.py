@@ -5,9 +5,8 @@ records what the split backward needs: its ``backward`` runs fa_backward_dq
 (delta = rowsum(dO * O) and dQ) and then fa_backward_dkdv (dK, dV) on the
 current stream -- the training-step integration that the MLX port of
 "Learning Metal with FlashAttention" lacks (its custom kernel has no
-backward).  Inputs are ``[B, H, N, D]`` bf16 CUDA tensors (D in {64, 128}
-when a gradient is needed; the forward alone also takes D = 192, 256);
-gradients come back in the inputs' dtype.  Nothing here computes attention:
+backward).  Inputs are ``[B, H, N, D]`` bf16 CUDA tensors, D any multiple of
+8 up to 256; gradients come back in the inputs' dtype.  Nothing here computes attention:
 every step runs in the library's kernels.
 """
 from __future__ import annotations

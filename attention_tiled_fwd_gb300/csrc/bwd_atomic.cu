@@ -254,6 +254,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t qmn_desc = sdesc_sw128(slot_addr + q_slot * L::kTileBytes, kBQ * 128, 1024);
             const uint64_t dmn_desc = sdesc_sw128(slot_addr + d_slot * L::kTileBytes, kBQ * 128, 1024);
             if (!(ok = warp_wait(&p_ready[b], (i >> 1) & 1, a.status, kSitePReady))) break;
+            // p_ready only proves S^T_i, hence Q_i, complete: wait for dO_i's copy as well (normally long
+            // since done; its slot cannot refill before this warp's own release after dK_i)
+            if (!(ok = warp_wait(&slot_full[d_slot], ((2 * i + 1) / NSLOT) & 1, a.status, kSiteSlotFull))) break;
             tc_fence_after();
             if (leader) {
 #pragma unroll

@@ -45,6 +45,12 @@
 // buffer has its own completion barrier (see dv_done below).  Q_i and dO_i
 // slots are released after dK_i, which is issued only after the compute warps
 // saw S^T_i and dP^T_i complete.
+//
+// Wider heads run the same kernel.  At D = 192, dV and dK take 384 columns, so
+// S^T and dP^T are single-buffered (NB = 1): S^T_{i+1} waits for dV_i and dP^T_{i+1}
+// for dK_i.  At D = 256 two CTAs share each key tile (grid y = the half): each
+// computes S^T and dP^T over all D (those products are repeated) and keeps one
+// 128-column half of dV and dK, which leaves the D = 128 layout of TMEM.
 #include "fa_internal.h"
 #include "sm100_ptx.cuh"
 #include <cmath>
@@ -57,12 +63,11 @@ constexpr int kBQ = kDkdvQRows;   // queries per tile
 constexpr int kComputeWG = 4;     // compute warpgroups, one 16-query range of every tile each
 constexpr int kFirstComputeWarp = 3;
 constexpr int kThreads = 32 * kFirstComputeWarp + 128 * kComputeWG;
-constexpr int kStatSlots = 4;     // query tiles' L / D in flight
 
 enum : int { kSiteKV = 41, kSiteSlotEmpty, kSiteSlotFull, kSiteSFull, kSitePReady, kSiteDpFull, kSiteDsReady,
              kSiteDone, kSiteFinal, kSiteDrain, kSiteStats, kSiteDvDone, kSiteDkDone };
 
-template <int D, int NSLOT>
+template <int D, int NSLOT, int kStatSlots>
 struct DkdvSmem {
     static constexpr int kKVBytes = kBN * D * 2;
     static constexpr int kTileBytes = kBQ * D * 2;  // one Q_i or dO_i tile
@@ -78,12 +83,15 @@ struct DkdvSmem {
     static constexpr int kAlloc = kTmemHolderOff + 16 + 1024;
 };
 
-template <int D, int NSLOT>
+// D: the contraction width the kernel is built for (64-column panels); DO: the columns of dV and dK one
+// CTA accumulates (D, or D / 2 with grid y choosing the half); NB: S^T / dP^T buffers in TMEM (2, or 1
+// where dV and dK leave no room); kStatSlots: query tiles whose L / D are staged ahead.
+template <int D, int DO, int NB, int NSLOT, int kStatSlots>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
                     BwdArgs a) {
-    using L = DkdvSmem<D, NSLOT>;
+    using L = DkdvSmem<D, NSLOT, kStatSlots>;
     constexpr int kPanels = D / 64;
     // Compute warpgroup g owns queries [g kSpan, (g+1) kSpan) of every tile and packs their bf16 P^T /
     // dS^T into the first kSpan / 2 columns of that range: 16-query k-step kk sits at column
@@ -92,8 +100,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kStepsPerWG = kSpan / 16;
     static_assert(kSpan == 16 || kSpan == 32, "16 or 32 queries per compute thread");
     constexpr uint32_t kTmemCols = 512;
-    constexpr uint32_t kColDV = 256, kColDK = 256 + D;
-    static_assert(256 + 2 * D <= 512, "TMEM budget");
+    // TMEM: S^T[b] = [64b, +64), dP^T[b] = [64 NB + 64b, +64), dV, dK (DO columns each)
+    constexpr uint32_t kColDP = 64 * NB, kColDV = 128 * NB, kColDK = 128 * NB + DO;
+    static_assert(128 * NB + 2 * DO <= 512, "TMEM budget");
+    static_assert(DO % 64 == 0 && D % DO == 0 && (NB == 1 || NB == 2), "dV / dK columns per CTA: whole panels");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -128,6 +138,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_q_total = (N + kBQ - 1) / kBQ;
     const int q_begin = a.causal ? (k_tile * kBN) / kBQ : 0;
     const int n_q = n_q_total - q_begin;  // >= 1
+    const int do0 = blockIdx.y * DO;      // first dV / dK column of this CTA
+    const int Dr = a.D;                   // row stride and real columns (<= D; the rest are zeros)
 
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
@@ -238,10 +250,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; ok && i < n_q; ++i) {
             const int q_slot = (2 * i) % NSLOT, q_round = (2 * i) / NSLOT;
             const int d_slot = (2 * i + 1) % NSLOT, d_round = (2 * i + 1) / NSLOT;
-            const uint32_t b = i & 1;
+            const uint32_t b = i % NB;
             if (!(ok = warp_wait(&slot_full[q_slot], q_round & 1, a.status, kSiteSlotFull))) break;
-            // buffer b last held P^T_{i-2}, read by dV_{i-2}
-            if (i >= 2 && !(ok = warp_wait(&dv_done[b], ((i - 2) >> 1) & 1, a.status, kSiteDvDone))) break;
+            // buffer b last held P^T_{i-NB}, read by dV_{i-NB}
+            if (i >= NB && !(ok = warp_wait(&dv_done[b], ((i - NB) / NB) & 1, a.status, kSiteDvDone))) break;
             tc_fence_after();
             const uint64_t q_desc = sdesc_sw128(slot_addr + q_slot * L::kTileBytes, 16, 1024);
             if (leader) {
@@ -253,14 +265,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
             if (!(ok = warp_wait(&slot_full[d_slot], d_round & 1, a.status, kSiteSlotFull))) break;
-            // buffer b last held dS^T_{i-2}, read by dK_{i-2}
-            if (i >= 2 && !(ok = warp_wait(&dk_done[b], ((i - 2) >> 1) & 1, a.status, kSiteDkDone))) break;
+            // buffer b last held dS^T_{i-NB}, read by dK_{i-NB}
+            if (i >= NB && !(ok = warp_wait(&dk_done[b], ((i - NB) / NB) & 1, a.status, kSiteDkDone))) break;
             tc_fence_after();
             const uint64_t do_desc = sdesc_sw128(slot_addr + d_slot * L::kTileBytes, 16, 1024);
             if (leader) {
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
-                    mma_ss(tmem + 128 + 64 * b, sdesc_add(v_desc, (ks >> 2) * (kBN * 128) + (ks & 3) * 32),
+                    mma_ss(tmem + kColDP + 64 * b, sdesc_add(v_desc, (ks >> 2) * (kBN * 128) + (ks & 3) * 32),
                            sdesc_add(do_desc, (ks >> 2) * (kBQ * 128) + (ks & 3) * 32), idesc_s, ks > 0);
                 mma_commit(&dp_full[b]);
             }
@@ -272,16 +284,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         warp_wait(a_final, 0, a.status, kSiteFinal);
     } else if (warp == 2) {
         // Issuer B: dV += P^T dO_i and dK += dS^T Q_i.
-        constexpr uint32_t idesc_g = idesc_bf16_f32(kBN, D, false, true);  // dV, dK: 128 x D
+        constexpr uint32_t idesc_g = idesc_bf16_f32(kBN, DO, false, true);  // dV, dK: 128 x DO
         const uint32_t slot_addr = smem_u32(slots);
         const bool leader = elect_one();
         bool ok = true;
         for (int i = 0; ok && i < n_q; ++i) {
-            const uint32_t b = i & 1;
+            const uint32_t b = i % NB;
             const int q_slot = (2 * i) % NSLOT, d_slot = (2 * i + 1) % NSLOT;
-            const uint64_t qmn_desc = sdesc_sw128(slot_addr + q_slot * L::kTileBytes, kBQ * 128, 1024);
-            const uint64_t dmn_desc = sdesc_sw128(slot_addr + d_slot * L::kTileBytes, kBQ * 128, 1024);
-            if (!(ok = warp_wait(&p_ready[b], (i >> 1) & 1, a.status, kSitePReady))) break;
+            // B = this CTA's DO columns of Q_i / dO_i (MN-major: whole 64-column panels from panel do0 / 64 on)
+            const uint32_t p0 = (do0 / 64) * (kBQ * 128);
+            const uint64_t qmn_desc = sdesc_sw128(slot_addr + q_slot * L::kTileBytes + p0, kBQ * 128, 1024);
+            const uint64_t dmn_desc = sdesc_sw128(slot_addr + d_slot * L::kTileBytes + p0, kBQ * 128, 1024);
+            if (!(ok = warp_wait(&p_ready[b], (i / NB) & 1, a.status, kSitePReady))) break;
+            // p_ready only proves S^T_i, hence Q_i, complete: dO_i's copy may still be in flight when the
+            // ring is short, so wait for its slot too (normally long since done; the slot cannot refill
+            // before this warp's own release after dK_i, so the phase is never two behind)
+            if (!(ok = warp_wait(&slot_full[d_slot], ((2 * i + 1) / NSLOT) & 1, a.status, kSiteSlotFull))) break;
             tc_fence_after();
             if (leader) {
 #pragma unroll
@@ -291,13 +309,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(&dv_done[b]);
             }
             __syncwarp();
-            if (!(ok = warp_wait(&ds_ready[b], (i >> 1) & 1, a.status, kSiteDsReady))) break;
+            if (!(ok = warp_wait(&ds_ready[b], (i / NB) & 1, a.status, kSiteDsReady))) break;
             tc_fence_after();
             if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < kBQ / 16; ++kk)
                     mma_ts(tmem + kColDK,
-                           tmem + 128 + 64 * b + (kk / kStepsPerWG) * kSpan + (kk % kStepsPerWG) * 8,
+                           tmem + kColDP + 64 * b + (kk / kStepsPerWG) * kSpan + (kk % kStepsPerWG) * 8,
                            sdesc_add(qmn_desc, kk * 2048), idesc_g, (i > 0 || kk > 0));
                 mma_commit(&dk_done[b]);
                 // S^T_i and dP^T_i (issuer A) completed before the compute warps produced dS^T_i, so after
@@ -321,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int i = 0; i < n_q; ++i) {
             const int qt = q_begin + i;
-            const int b = i & 1;
+            const int b = i % NB;
             const int ss = i % kStatSlots;
             ok = mbar_wait(&stat_full[ss], (i / kStatSlots) & 1, a.status, kSiteStats);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -332,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool need_mask = (q0 + kHalf > N) || (a.causal && key > q0) || (key >= N);
             const bool any_mask = __any_sync(0xffffffffu, need_mask);
 
-            ok = mbar_wait(&s_full[b], (i >> 1) & 1, a.status, kSiteSFull);
+            ok = mbar_wait(&s_full[b], (i / NB) & 1, a.status, kSiteSFull);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
             // P^T of this thread's queries: bf16 pairs for the dV operand, fp32 pairs kept for dS^T below.
@@ -375,12 +393,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             warp_arrive(&p_ready[b]);
 
-            ok = mbar_wait(&dp_full[b], (i >> 1) & 1, a.status, kSiteDpFull);
+            ok = mbar_wait(&dp_full[b], (i / NB) & 1, a.status, kSiteDpFull);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
             {
                 uint32_t raw[kHalf], dsk[kHalf / 2];
-                tmem_ld_n<kHalf>(tmem + lane_base + 128 + 64 * b + g * kHalf, raw);
+                tmem_ld_n<kHalf>(tmem + lane_base + kColDP + 64 * b + g * kHalf, raw);
                 tmem_wait_ld();
 #pragma unroll
                 for (int q4 = 0; q4 < kHalf / 4; ++q4) {
@@ -395,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                f2_pack(d4.z, d4.w)),
                         p2[2 * q4 + 1]));
                 }
-                tmem_st_n<kHalf / 2>(tmem + lane_base + 128 + 64 * b + g * kHalf, dsk);
+                tmem_st_n<kHalf / 2>(tmem + lane_base + kColDP + 64 * b + g * kHalf, dsk);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -410,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const bool valid = key < N;
             // the first half of the warpgroups writes dV, the second dK; each its share of the D columns
-            constexpr int kCols = D / (kComputeWG / 2);
+            constexpr int kCols = DO / (kComputeWG / 2);
             const bool is_dv = g < kComputeWG / 2;
             const int c0 = (g % (kComputeWG / 2)) * kCols;
             const uint32_t col = (is_dv ? kColDV : kColDK) + c0;
@@ -424,11 +442,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!valid) continue;
 #pragma unroll
                 for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * osc);
+                const int gc = do0 + c0 + ch * 32;  // first global column of this chunk
                 if (a.grad_bf16) {
                     uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(outp) +
-                                                           ((size_t)bh * N + key) * D + c0 + ch * 32);
+                                                           ((size_t)bh * N + key) * Dr + gc);
 #pragma unroll
                     for (int v4 = 0; v4 < 4; ++v4) {
+                        if (gc + 8 * v4 >= Dr) break;
                         uint4 w;
                         w.x = pack_bf16x2(__uint_as_float(v[v4 * 8 + 0]), __uint_as_float(v[v4 * 8 + 1]));
                         w.y = pack_bf16x2(__uint_as_float(v[v4 * 8 + 2]), __uint_as_float(v[v4 * 8 + 3]));
@@ -438,10 +458,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 } else {
                     float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(outp) +
-                                                             ((size_t)bh * N + key) * D + c0 + ch * 32);
+                                                             ((size_t)bh * N + key) * Dr + gc);
 #pragma unroll
                     for (int v4 = 0; v4 < 8; ++v4)
-                        dst[v4] = make_float4(__uint_as_float(v[v4 * 4 + 0]), __uint_as_float(v[v4 * 4 + 1]),
+                        if (gc + 4 * v4 < Dr) dst[v4] = make_float4(__uint_as_float(v[v4 * 4 + 0]), __uint_as_float(v[v4 * 4 + 1]),
                                               __uint_as_float(v[v4 * 4 + 2]), __uint_as_float(v[v4 * 4 + 3]));
                 }
             }
@@ -456,15 +476,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D, int NSLOT>
+template <int D, int DO, int NB, int NSLOT, int STATS>
 cudaError_t launch_spec(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                         const CUtensorMap &tdo, cudaStream_t s) {
-    using L = DkdvSmem<D, NSLOT>;
+    using L = DkdvSmem<D, NSLOT, STATS>;
     static_assert(L::kAlloc <= 232448, "shared memory budget");
-    auto kern = bwd_dkdv_kernel<D, NSLOT>;
+    auto kern = bwd_dkdv_kernel<D, DO, NB, NSLOT, STATS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
-    dim3 grid(((a.N + kBN - 1) / kBN) * a.H * a.B);
+    dim3 grid(((a.N + kBN - 1) / kBN) * a.H * a.B, D / DO);
     kern<<<grid, kThreads, L::kAlloc, s>>>(tq, tk, tv, tdo, a);
     return cudaGetLastError();
 }
@@ -473,8 +493,10 @@ cudaError_t launch_spec(const BwdArgs &a, const CUtensorMap &tq, const CUtensorM
 
 cudaError_t launch_bwd_dkdv(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             const CUtensorMap &tdo, cudaStream_t s) {
-    switch (a.D) {
-        case 128: return launch_spec<128, 8>(a, tq, tk, tv, tdo, s);
+    switch (kernel_head_dim(a.D)) {
+        case 128: return launch_spec<128, 128, 2, 8, 4>(a, tq, tk, tv, tdo, s);
+        case 192: return launch_spec<192, 192, 1, 5, 4>(a, tq, tk, tv, tdo, s);
+        case 256: return launch_spec<256, 128, 2, 3, 3>(a, tq, tk, tv, tdo, s);
         default: return cudaErrorInvalidValue;
     }
 }

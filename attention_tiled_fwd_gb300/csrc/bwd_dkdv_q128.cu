@@ -246,6 +246,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t qmn_desc = sdesc_sw128(slot_addr + q_slot * L::kTileBytes, kBQ * 128, 1024);
             const uint64_t dmn_desc = sdesc_sw128(slot_addr + d_slot * L::kTileBytes, kBQ * 128, 1024);
             if (!(ok = warp_wait(&p_ready[b], (i >> 1) & 1, a.status, kSitePReady))) break;
+            // p_ready only proves S^T_i, hence Q_i, complete: wait for dO_i's copy as well (normally long
+            // since done; its slot cannot refill before this warp's own release after dK_i)
+            if (!(ok = warp_wait(&slot_full[d_slot], ((2 * i + 1) / kNSlot) & 1, a.status, kSiteSlotFull))) break;
             tc_fence_after();
             if (leader) {
 #pragma unroll
@@ -381,14 +384,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t v[32];
             tmem_ld32(tmem + lane_base + (is_dv ? kColDV : kColDK) + c0, v);
             tmem_wait_ld();
+            // row stride and real columns: the caller's D (a multiple of 8, at most 64)
+            const int Dr = a.D;
             if (valid) {
 #pragma unroll
                 for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * osc);
                 if (a.grad_bf16) {
                     uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(outp) +
-                                                           ((size_t)bh * N + key) * kD + c0);
+                                                           ((size_t)bh * N + key) * Dr + c0);
 #pragma unroll
                     for (int v4 = 0; v4 < 4; ++v4) {
+                        if (c0 + 8 * v4 >= Dr) break;
                         uint4 o4;
                         o4.x = pack_bf16x2(__uint_as_float(v[v4 * 8 + 0]), __uint_as_float(v[v4 * 8 + 1]));
                         o4.y = pack_bf16x2(__uint_as_float(v[v4 * 8 + 2]), __uint_as_float(v[v4 * 8 + 3]));
@@ -398,10 +404,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 } else {
                     float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(outp) +
-                                                             ((size_t)bh * N + key) * kD + c0);
+                                                             ((size_t)bh * N + key) * Dr + c0);
 #pragma unroll
                     for (int v4 = 0; v4 < 8; ++v4)
-                        dst[v4] = make_float4(__uint_as_float(v[v4 * 4 + 0]), __uint_as_float(v[v4 * 4 + 1]),
+                        if (c0 + 4 * v4 < Dr) dst[v4] = make_float4(__uint_as_float(v[v4 * 4 + 0]), __uint_as_float(v[v4 * 4 + 1]),
                                               __uint_as_float(v[v4 * 4 + 2]), __uint_as_float(v[v4 * 4 + 3]));
                 }
             }
@@ -422,7 +428,7 @@ cudaError_t launch_bwd_dkdv_q128(const BwdArgs &a, const CUtensorMap &tq, const 
                                  const CUtensorMap &tv, const CUtensorMap &tdo, cudaStream_t s) {
     using L = Q128Smem;
     static_assert(L::kAlloc <= 232448, "shared memory budget");
-    if (a.D != kD) return cudaErrorInvalidValue;
+    if (kernel_head_dim(a.D) != kD) return cudaErrorInvalidValue;
     auto kern = bwd_dkdv_q128_kernel;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;

@@ -42,6 +42,13 @@
 // waiting for dQ_{j-2}, the previous reader of dS[j % 2]; S_{j+2} / dP_{j+2}
 // overwrite S[b] / dP[b] only after the compute warps finished tile j.  K_j is
 // released after dQ_j, which is issued only after S_j completed.
+//
+// Wider heads (D = 192, 256) run the same kernel with two changes.  Q stays in
+// shared memory and S = Q K_j^T is an SS product, because dQ needs D (192) or
+// its share (128) of the 512 columns.  At D = 256, dQ alone would fill half of
+// TMEM, so two CTAs share each query tile: each computes S and dP over all D
+// (those products are repeated) and keeps one 128-column half of dQ (grid y =
+// the half).  At D = 192 one CTA keeps all 192 columns of dQ.
 #include "fa_internal.h"
 #include "sm100_ptx.cuh"
 #include <cmath>
@@ -73,7 +80,10 @@ struct DqSmem {
     static constexpr int kAlloc = kTmemHolderOff + 16 + 1024;
 };
 
-template <int D, int NSLOT>
+// D: the contraction width the kernel is built for (64-column panels); DQ: the columns of dQ one
+// CTA accumulates (D, or D / 2 with grid y choosing the half); QT: Q kept in TMEM as the A operand of
+// S (else S reads Q from shared memory).
+template <int D, int DQ, bool QT, int NSLOT>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
@@ -81,8 +91,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     using L = DqSmem<D, NSLOT>;
     constexpr int kPanels = D / 64;
     constexpr uint32_t kTmemCols = 512;
-    constexpr uint32_t kColDQ = 256, kColDS = 256 + D, kColQ = kColDS + 64;
-    static_assert(kColQ + D / 2 <= 512, "TMEM budget");
+    constexpr uint32_t kColDQ = 256, kColDS = 256 + DQ, kColQ = kColDS + 64;
+    static_assert(kColQ + (QT ? D / 2 : 0) <= 512, "TMEM budget");
+    static_assert(DQ % 64 == 0 && D % DQ == 0, "dQ columns per CTA: whole panels");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -109,6 +120,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int N = a.N;
     const int kv_end = a.causal ? min(N, (q_tile + 1) * kBM) : N;
     const int n_kv = (kv_end + kBN - 1) / kBN;  // >= 1
+    const int dq0 = blockIdx.y * DQ;            // first dQ column of this CTA
+    const int Dr = a.D;                         // row stride and real columns (<= D; the rest are zeros)
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
@@ -177,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t do_desc = sdesc_sw128(smem_u32(do_s), 16, 1024);
         const uint32_t slot_addr = smem_u32(slots);
         const bool leader = elect_one();
-        bool ok = warp_wait(q_full, 0, a.status, kSiteQ) && warp_wait(qt_ready, 0, a.status, kSiteQt);
+        bool ok = warp_wait(q_full, 0, a.status, kSiteQ) && (!QT || warp_wait(qt_ready, 0, a.status, kSiteQt));
         tc_fence_after();
         for (int j = 0; ok && j < n_kv; ++j) {
             const int k_slot = (2 * j) % NSLOT, k_round = (2 * j) / NSLOT;
@@ -192,9 +205,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t v_desc = sdesc_sw128(slot_addr + v_slot * L::kTileBytes, 16, 1024);
             if (leader) {
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks)
-                    mma_ts(tmem + 64 * b, tmem + kColQ + ks * 8,
-                           sdesc_add(k_desc, (ks >> 2) * (kBN * 128) + (ks & 3) * 32), idesc_sq, ks > 0);
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    if constexpr (QT)
+                        mma_ts(tmem + 64 * b, tmem + kColQ + ks * 8,
+                               sdesc_add(k_desc, (ks >> 2) * (kBN * 128) + (ks & 3) * 32), idesc_sq, ks > 0);
+                    else
+                        mma_ss(tmem + 64 * b, sdesc_add(q_desc, (ks >> 2) * (kBM * 128) + (ks & 3) * 32),
+                               sdesc_add(k_desc, (ks >> 2) * (kBN * 128) + (ks & 3) * 32), idesc_sq, ks > 0);
+                }
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
                     mma_ss(tmem + 128 + 64 * b, sdesc_add(do_desc, (ks >> 2) * (kBM * 128) + (ks & 3) * 32),
@@ -210,14 +228,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         warp_wait(a_final, 0, a.status, kSiteFinal);
     } else if (warp == 2) {
         // Issuer B: dQ += dS_j K_j.
-        constexpr uint32_t idesc_dq = idesc_bf16_f32(kBM, D, false, true);  // dQ += dS K: 128 x D
+        constexpr uint32_t idesc_dq = idesc_bf16_f32(kBM, DQ, false, true);  // dQ += dS K: 128 x DQ
         const uint32_t slot_addr = smem_u32(slots);
         const bool leader = elect_one();
         bool ok = true;
         for (int j = 0; ok && j < n_kv; ++j) {
             const uint32_t b = j & 1;
             const int k_slot = (2 * j) % NSLOT;
-            const uint64_t kmn_desc = sdesc_sw128(slot_addr + k_slot * L::kTileBytes, kBN * 128, 1024);
+            // B = this CTA's DQ columns of K_j (MN-major: whole 64-column panels from panel dq0 / 64 on)
+            const uint64_t kmn_desc =
+                sdesc_sw128(slot_addr + k_slot * L::kTileBytes + (dq0 / 64) * (kBN * 128), kBN * 128, 1024);
             if (!(ok = warp_wait(&ds_full[b], (j >> 1) & 1, a.status, kSiteDsFull))) break;
             tc_fence_after();
             if (leader) {
@@ -250,11 +270,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         float delta = 0.f;
         if (valid) {
             const uint4 *orow = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.o) +
-                                                                ((size_t)bh * N + row) * D + g * kDCols);
+                                                                ((size_t)bh * N + row) * Dr + g * kDCols);
             const uint4 *drow = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.dO) +
-                                                                ((size_t)bh * N + row) * D + g * kDCols);
+                                                                ((size_t)bh * N + row) * Dr + g * kDCols);
 #pragma unroll 4
             for (int i = 0; i < kDCols / 8; ++i) {
+                if (g * kDCols + 8 * i >= Dr) break;
                 const uint4 ov = orow[i], dv = drow[i];
                 const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, dw[4] = {dv.x, dv.y, dv.z, dv.w};
 #pragma unroll
@@ -272,14 +293,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         delta = 0.f;
 #pragma unroll
         for (int t = 0; t < kComputeWG; ++t) delta += delta_s[t * kBM + r];
-        if (valid && g == 0) a.delta[(size_t)bh * N + row] = delta;
+        if (valid && g == 0 && blockIdx.y == 0) a.delta[(size_t)bh * N + row] = delta;
         const int lim = a.causal ? min(N - 1, row) : N - 1;  // last visible key
         // Q rows into TMEM as bf16 pairs, one 64-column panel per warpgroup
         // (row r of a panel is 128 B at r * 128, its 16-byte chunk k stored at k ^ (r % 8))
         {
-            bool qok = mbar_wait(q_full, 0, a.status, kSiteQ);
+            bool qok = !QT || mbar_wait(q_full, 0, a.status, kSiteQ);
             if (!__all_sync(0xffffffffu, qok)) qok = false;
-            if (qok) {
+            if (QT && qok) {
 #pragma unroll
                 for (int p = g; p < kPanels; p += kComputeWG) {
                     const uint8_t *panel = q_s + p * (kBM * 128) + r * 128;
@@ -344,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok) {
             tc_fence_after();
-            constexpr int kCols = D / kComputeWG;  // this warpgroup's columns of dQ
+            constexpr int kCols = DQ / kComputeWG;  // this warpgroup's columns of dQ
             constexpr int kChunk = kCols < 32 ? kCols : 32;
             uint32_t v[kChunk];
 #pragma unroll
@@ -357,9 +378,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (valid) {
                     if (a.grad_bf16) {
                         uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.dq) +
-                                                               ((size_t)bh * N + row) * D + col);
+                                                               ((size_t)bh * N + row) * Dr + dq0 + col);
 #pragma unroll
                         for (int v4 = 0; v4 < kChunk / 8; ++v4) {
+                            if (dq0 + col + 8 * v4 >= Dr) break;
                             uint4 w;
                             w.x = pack_bf16x2(__uint_as_float(v[v4 * 8 + 0]), __uint_as_float(v[v4 * 8 + 1]));
                             w.y = pack_bf16x2(__uint_as_float(v[v4 * 8 + 2]), __uint_as_float(v[v4 * 8 + 3]));
@@ -369,10 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     } else {
                         float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.dq) +
-                                                                 ((size_t)bh * N + row) * D + col);
+                                                                 ((size_t)bh * N + row) * Dr + dq0 + col);
 #pragma unroll
                         for (int v4 = 0; v4 < kChunk / 4; ++v4)
-                            dst[v4] = make_float4(__uint_as_float(v[v4 * 4 + 0]), __uint_as_float(v[v4 * 4 + 1]),
+                            if (dq0 + col + 4 * v4 < Dr) dst[v4] = make_float4(__uint_as_float(v[v4 * 4 + 0]), __uint_as_float(v[v4 * 4 + 1]),
                                                   __uint_as_float(v[v4 * 4 + 2]), __uint_as_float(v[v4 * 4 + 3]));
                     }
                 }
@@ -388,15 +410,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D, int NSLOT>
+template <int D, int DQ, bool QT, int NSLOT>
 cudaError_t launch_spec(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                         const CUtensorMap &tdo, cudaStream_t s) {
     using L = DqSmem<D, NSLOT>;
     static_assert(L::kAlloc <= 232448, "shared memory budget");
-    auto kern = bwd_dq_kernel<D, NSLOT>;
+    auto kern = bwd_dq_kernel<D, DQ, QT, NSLOT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
-    dim3 grid(((a.N + kBM - 1) / kBM) * a.H * a.B);
+    dim3 grid(((a.N + kBM - 1) / kBM) * a.H * a.B, D / DQ);
     kern<<<grid, kThreads, L::kAlloc, s>>>(tq, tk, tv, tdo, a);
     return cudaGetLastError();
 }
@@ -405,8 +427,10 @@ cudaError_t launch_spec(const BwdArgs &a, const CUtensorMap &tq, const CUtensorM
 
 cudaError_t launch_bwd_dq(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                           const CUtensorMap &tdo, cudaStream_t s) {
-    switch (a.D) {
-        case 128: return launch_spec<128, 8>(a, tq, tk, tv, tdo, s);
+    switch (kernel_head_dim(a.D)) {
+        case 128: return launch_spec<128, 128, true, 8>(a, tq, tk, tv, tdo, s);
+        case 192: return launch_spec<192, 192, false, 5>(a, tq, tk, tv, tdo, s);
+        case 256: return launch_spec<256, 128, false, 3>(a, tq, tk, tv, tdo, s);
         default: return cudaErrorInvalidValue;
     }
 }

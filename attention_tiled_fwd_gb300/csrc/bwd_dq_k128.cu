@@ -243,14 +243,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         // D_i = sum_d dO_id O_id for this thread's row, while the producer's TMA brings in Q and dO:
         // warpgroup g sums columns [16g, 16g + 16); the partial sums meet in shared memory and every
         // warpgroup adds them in the same order.
+        // Row stride and real columns: the caller's D (a multiple of 8, at most 64; TMA fills the rest of
+        // the 64-column panels with zeros, which add nothing).
+        const int Dr = a.D;
         float delta = 0.f;
         if (valid) {
             const uint4 *orow = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.o) +
-                                                                ((size_t)bh * N + row) * kD + 16 * g);
+                                                                ((size_t)bh * N + row) * Dr + 16 * g);
             const uint4 *drow = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.dO) +
-                                                                ((size_t)bh * N + row) * kD + 16 * g);
+                                                                ((size_t)bh * N + row) * Dr + 16 * g);
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
+                if (16 * g + 8 * i >= Dr) break;
                 const uint4 ov = orow[i], dv = drow[i];
                 const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, dw[4] = {dv.x, dv.y, dv.z, dv.w};
 #pragma unroll
@@ -355,9 +359,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int t = 0; t < 16; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * a.scale);
                 if (a.grad_bf16) {
                     uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.dq) +
-                                                           ((size_t)bh * N + row) * kD + 16 * g);
+                                                           ((size_t)bh * N + row) * Dr + 16 * g);
 #pragma unroll
                     for (int v4 = 0; v4 < 2; ++v4) {
+                        if (16 * g + 8 * v4 >= Dr) break;
                         uint4 o4;
                         o4.x = pack_bf16x2(__uint_as_float(v[v4 * 8 + 0]), __uint_as_float(v[v4 * 8 + 1]));
                         o4.y = pack_bf16x2(__uint_as_float(v[v4 * 8 + 2]), __uint_as_float(v[v4 * 8 + 3]));
@@ -367,10 +372,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 } else {
                     float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.dq) +
-                                                             ((size_t)bh * N + row) * kD + 16 * g);
+                                                             ((size_t)bh * N + row) * Dr + 16 * g);
 #pragma unroll
                     for (int v4 = 0; v4 < 4; ++v4)
-                        dst[v4] = make_float4(__uint_as_float(v[v4 * 4 + 0]), __uint_as_float(v[v4 * 4 + 1]),
+                        if (16 * g + 4 * v4 < Dr) dst[v4] = make_float4(__uint_as_float(v[v4 * 4 + 0]), __uint_as_float(v[v4 * 4 + 1]),
                                               __uint_as_float(v[v4 * 4 + 2]), __uint_as_float(v[v4 * 4 + 3]));
                 }
             }
@@ -391,7 +396,7 @@ cudaError_t launch_bwd_dq_k128(const BwdArgs &a, const CUtensorMap &tq, const CU
                                const CUtensorMap &tdo, cudaStream_t s) {
     using L = K128Smem;
     static_assert(L::kAlloc <= 232448, "shared memory budget");
-    if (a.D != kD) return cudaErrorInvalidValue;
+    if (kernel_head_dim(a.D) != kD) return cudaErrorInvalidValue;
     auto kern = bwd_dq_k128_kernel;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;

@@ -369,14 +369,14 @@ std::mutex g_scratch_mu;
 
 int decode_max_rows(int) { return kMaxRows; }
 
-void decode_split(int B, int H, int n_q, int N, int D, int *splits, int *chunk) {
+void decode_split(int B, int H, int n_q, int N, int D, int num_sms, int *splits, int *chunk) {
     // Pick the number of key chunks per (batch, head) that minimises
     //   waves(s) * (keys per chunk + a fixed cost per CTA, counted as 64 keys),
-    // waves(s) = ceil(CTAs / resident CTAs), CTAs = B * H * row blocks * s.
+    // waves(s) = ceil(CTAs / resident CTAs), CTAs = B * H * row blocks * s, for a device of num_sms SMs.
     const int rows = n_q < kRowBlock ? n_q : kRowBlock;
     const long long units = (long long)B * H * ((n_q + rows - 1) / rows);
     const int step = D == 256 ? StreamCfg<256>::kStep : D == 128 ? StreamCfg<128>::kStep : StreamCfg<64>::kStep;
-    const long long cap = (long long)kNumSms * stream_ctas_per_sm(rows);
+    const long long cap = (long long)(num_sms > 0 ? num_sms : kNumSms) * stream_ctas_per_sm(rows);
     const long long max_s = (N + step - 1) / step;
     const long long s_hi = max_s < 4 * cap ? max_s : 4 * cap;
     long long best_s = 1;
@@ -398,9 +398,9 @@ void decode_split(int B, int H, int n_q, int N, int D, int *splits, int *chunk) 
     *splits = (int)((N + c - 1) / c);
 }
 
-size_t decode_workspace_bytes(int B, int H, int n_q, int N, int D) {
+size_t decode_workspace_bytes(int B, int H, int n_q, int N, int D, int num_sms) {
     int splits, chunk;
-    decode_split(B, H, n_q, N, D, &splits, &chunk);
+    decode_split(B, H, n_q, N, D, num_sms, &splits, &chunk);
     return sizeof(float) * (size_t)B * H * splits * n_q * (size_t)(D + 2);
 }
 

@@ -121,6 +121,22 @@ int encode_bf16_3d(CUtensorMap *map, const void *base, int BH, int N, int D, int
 
 float log2e() { return 1.4426950408889634f; }
 
+// bf16 head dimensions the tensor-core kernels take: a multiple of 8 (whole 16-byte units per row, as
+// the TMA needs for the row stride) up to 256; each runs on the kernel of width kernel_head_dim(D).
+bool bf16_head_dim_ok(int D) { return D >= 8 && D <= 256 && D % 8 == 0; }
+
+// SM count of the current device for the host-side size queries, which must also answer without a
+// usable device (they make no launch): the GB300 count when it cannot be read.
+int current_num_sms() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess) {
+        cudaGetLastError();
+        return kNumSms;
+    }
+    return sms > 0 ? sms : kNumSms;
+}
+
 }  // namespace
 }  // namespace fa
 
@@ -131,9 +147,9 @@ extern "C" int fa_forward(const void *q, const void *k, const void *v, void *o, 
     int rc = check_shape(B, H, N, D, scale);
     if (rc != FA_OK) return rc;
     if (dtype == FA_BF16) {
-        if (D != 64 && D != 128 && D != 192 && D != 256) return FA_ERR_HEAD_DIM;
+        if (!bf16_head_dim_ok(D)) return FA_ERR_HEAD_DIM;
     } else if (dtype == FA_F32) {
-        if (D % 32 != 0 || D > 256) return FA_ERR_HEAD_DIM;
+        if (D % 4 != 0 || D > 256) return FA_ERR_HEAD_DIM;
     } else {
         return FA_ERR_DTYPE;
     }
@@ -151,7 +167,7 @@ extern "C" int fa_forward(const void *q, const void *k, const void *v, void *o, 
         e = launch_fwd_f32(a, s);
     } else {
         CUtensorMap tq, tk, tv;
-        const int bn = fwd_block_n(D);
+        const int bn = fwd_block_n(kernel_head_dim(D));
         if (encode_bf16_3d(&tq, q, B * H, N, D, 128) != FA_OK || encode_bf16_3d(&tk, k, B * H, N, D, bn) != FA_OK ||
             encode_bf16_3d(&tv, v, B * H, N, D, bn) != FA_OK)
             return FA_ERR_CUDA;
@@ -168,7 +184,7 @@ extern "C" int fa_backward_dq(const void *q, const void *k, const void *v, const
     if (dtype != FA_BF16 && dtype != FA_F32) return FA_ERR_DTYPE;
     if (grad_dtype != FA_BF16 && grad_dtype != FA_F32) return FA_ERR_DTYPE;
     if (dtype != FA_BF16) return FA_ERR_DTYPE;  // the split backward runs on bf16 inputs
-    if (D != 64 && D != 128) return FA_ERR_HEAD_DIM;
+    if (!bf16_head_dim_ok(D)) return FA_ERR_HEAD_DIM;
     rc = check_ptrs({q, k, v, o, dO, lse, delta, dq});
     if (rc != FA_OK) return rc;
     int dev;
@@ -178,15 +194,16 @@ extern "C" int fa_backward_dq(const void *q, const void *k, const void *v, const
     BwdArgs a{q, k, v, o, dO, lse, delta, dq, nullptr, nullptr, B, H, N, D, scale, scale * log2e(),
               causal ? 1 : 0, grad_dtype == FA_BF16 ? 1 : 0, st->status_word};
     CUtensorMap tq, tk, tv, tdo;
-    // D = 64 runs the 128-key-tile kernel (its score products are N = 128 MMAs); D = 128 the 64-key one
-    const int kv_rows = D == 64 ? 128 : kDqKRows;
+    // D <= 64 runs the 128-key-tile kernel (its score products are N = 128 MMAs); wider heads the 64-key one
+    const int Dk = kernel_head_dim(D);
+    const int kv_rows = Dk == 64 ? 128 : kDqKRows;
     if (encode_bf16_3d(&tq, q, B * H, N, D, 128) != FA_OK ||
         encode_bf16_3d(&tk, k, B * H, N, D, kv_rows) != FA_OK ||
         encode_bf16_3d(&tv, v, B * H, N, D, kv_rows) != FA_OK ||
         encode_bf16_3d(&tdo, dO, B * H, N, D, 128) != FA_OK)
         return FA_ERR_CUDA;
-    cudaError_t e = D == 64 ? launch_bwd_dq_k128(a, tq, tk, tv, tdo, reinterpret_cast<cudaStream_t>(stream))
-                            : launch_bwd_dq(a, tq, tk, tv, tdo, reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e = Dk == 64 ? launch_bwd_dq_k128(a, tq, tk, tv, tdo, reinterpret_cast<cudaStream_t>(stream))
+                             : launch_bwd_dq(a, tq, tk, tv, tdo, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -198,7 +215,7 @@ extern "C" int fa_backward_dkdv(const void *q, const void *k, const void *v, con
     if (dtype != FA_BF16 && dtype != FA_F32) return FA_ERR_DTYPE;
     if (grad_dtype != FA_BF16 && grad_dtype != FA_F32) return FA_ERR_DTYPE;
     if (dtype != FA_BF16) return FA_ERR_DTYPE;
-    if (D != 64 && D != 128) return FA_ERR_HEAD_DIM;
+    if (!bf16_head_dim_ok(D)) return FA_ERR_HEAD_DIM;
     rc = check_ptrs({q, k, v, dO, lse, delta, dk, dv});
     if (rc != FA_OK) return rc;
     int dev;
@@ -208,14 +225,15 @@ extern "C" int fa_backward_dkdv(const void *q, const void *k, const void *v, con
     BwdArgs a{q, k, v, nullptr, dO, lse, const_cast<float *>(delta), nullptr, dk, dv, B, H, N, D, scale,
               scale * log2e(), causal ? 1 : 0, grad_dtype == FA_BF16 ? 1 : 0, st->status_word};
     CUtensorMap tq, tk, tv, tdo;
-    // D = 64 runs the 128-query-tile kernel (its score products are N = 128 MMAs); D = 128 the 64-query one
-    const int q_rows = D == 64 ? 128 : kDkdvQRows;
+    // D <= 64 runs the 128-query-tile kernel (its score products are N = 128 MMAs); wider heads the 64-query one
+    const int Dk = kernel_head_dim(D);
+    const int q_rows = Dk == 64 ? 128 : kDkdvQRows;
     if (encode_bf16_3d(&tq, q, B * H, N, D, q_rows) != FA_OK ||
         encode_bf16_3d(&tk, k, B * H, N, D, 128) != FA_OK || encode_bf16_3d(&tv, v, B * H, N, D, 128) != FA_OK ||
         encode_bf16_3d(&tdo, dO, B * H, N, D, q_rows) != FA_OK)
         return FA_ERR_CUDA;
-    cudaError_t e = D == 64 ? launch_bwd_dkdv_q128(a, tq, tk, tv, tdo, reinterpret_cast<cudaStream_t>(stream))
-                            : launch_bwd_dkdv(a, tq, tk, tv, tdo, reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e = Dk == 64 ? launch_bwd_dkdv_q128(a, tq, tk, tv, tdo, reinterpret_cast<cudaStream_t>(stream))
+                             : launch_bwd_dkdv(a, tq, tk, tv, tdo, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -261,7 +279,7 @@ extern "C" int fa_decode_workspace_bytes(int B, int H, int n_q, int N, int D, si
     if (!bytes) return FA_ERR_NULL;
     int rc = check_decode(B, H, n_q, N, D, 1.f);
     if (rc != FA_OK) return rc;
-    *bytes = decode_workspace_bytes(B, H, n_q, N, D);
+    *bytes = decode_workspace_bytes(B, H, n_q, N, D, current_num_sms());
     return FA_OK;
 }
 
@@ -272,14 +290,14 @@ extern "C" int fa_decode(const void *q, const void *k, const void *v, void *o, f
     if (rc != FA_OK) return rc;
     rc = check_ptrs({q, k, v, o, lse, workspace});
     if (rc != FA_OK) return rc;
-    if (workspace_bytes < decode_workspace_bytes(B, H, n_q, N, D)) return FA_ERR_WORKSPACE;
     int dev;
     DeviceState *st;
     rc = device_state(&dev, &st);
     if (rc != FA_OK) return rc;
+    if (workspace_bytes < decode_workspace_bytes(B, H, n_q, N, D, st->num_sms)) return FA_ERR_WORKSPACE;
     DecodeArgs a{q, k, v, o, lse, static_cast<float *>(workspace), B, H, n_q, N, D, 0, 0, scale * log2e(),
                  causal ? 1 : 0};
-    decode_split(B, H, n_q, N, D, &a.splits, &a.chunk);
+    decode_split(B, H, n_q, N, D, st->num_sms, &a.splits, &a.chunk);
     cudaError_t e = launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -292,17 +310,19 @@ extern "C" int fa_decode_noalloc(const void *q, const void *k, const void *v, vo
                                  int n_q, int N, int D, float scale, int causal, void *stream) {
     int rc = check_decode(B, H, n_q, N, D, scale);
     if (rc != FA_OK) return rc;
-    if (decode_workspace_bytes(B, H, n_q, N, D) > kDecodeScratchBytes) return FA_ERR_SCRATCH_LIMIT;
+    if (decode_workspace_bytes(B, H, n_q, N, D, current_num_sms()) > kDecodeScratchBytes)
+        return FA_ERR_SCRATCH_LIMIT;
     rc = check_ptrs({q, k, v, o, lse});
     if (rc != FA_OK) return rc;
     int dev;
     DeviceState *st;
     rc = device_state(&dev, &st);
     if (rc != FA_OK) return rc;
+    if (decode_workspace_bytes(B, H, n_q, N, D, st->num_sms) > kDecodeScratchBytes) return FA_ERR_SCRATCH_LIMIT;
     float *scratch = nullptr;
     if (decode_static_scratch(&scratch) != cudaSuccess) return FA_ERR_CUDA;
     DecodeArgs a{q, k, v, o, lse, scratch, B, H, n_q, N, D, 0, 0, scale * log2e(), causal ? 1 : 0};
-    decode_split(B, H, n_q, N, D, &a.splits, &a.chunk);
+    decode_split(B, H, n_q, N, D, st->num_sms, &a.splits, &a.chunk);
     cudaError_t e = launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

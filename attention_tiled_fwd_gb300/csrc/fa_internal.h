@@ -11,11 +11,10 @@ namespace fa {
 // ring depth, keyed by head dimension.  Picked so that the score, P and O
 // buffers fit the 512 TMEM columns and the staged tiles fill (but do not
 // exceed) shared memory.
-//   D = 64, 128: two 128-row query tiles per CTA (fwd_bf16_pair.cu); TMEM per
-//                tile S 128 (P over its first 64) + O D columns; shared memory
-//                2 Q tiles + ring.  Non-causal D = 128 instead runs the
-//                one-tile kernel of fwd_bf16.cu with 128-key tiles (S
-//                double-buffered, 5-slot ring), which measured faster there.
+//   D = 64, 128: two 128-row query tiles per CTA (fwd_bf16_pair.cu), causal
+//                and non-causal, on a persistent grid of one CTA per SM; TMEM
+//                per tile S 128 (P over its first 64) + O D columns; shared
+//                memory 2 Q tiles + ring.
 //   D = 192, 256: one 128-row query tile, two softmax warpgroups splitting
 //                the columns (fwd_bf16.cu); TMEM S 2x64 + P 2x32 + O D (one
 //                N = D accumulator, D-blocked shared-memory panels).
@@ -93,7 +92,7 @@ cudaError_t launch_bwd_atomic(const BwdArgs &a, void *dq_out, const CUtensorMap 
                               const CUtensorMap &tv, const CUtensorMap &tdo, cudaStream_t s);
 
 // Decode (few query rows against a long key range), split over the keys.
-constexpr int kNumSms = 152;  // GB300
+constexpr int kNumSms = 152;  // GB300; used only when the device's own SM count cannot be read
 
 struct DecodeArgs {
     const void *q, *k, *v;  // q [B, H, n_q, D]; k, v [B, H, N, D]; bf16
@@ -107,8 +106,9 @@ struct DecodeArgs {
 };
 
 int decode_max_rows(int D);
-void decode_split(int B, int H, int n_q, int N, int D, int *splits, int *chunk);
-size_t decode_workspace_bytes(int B, int H, int n_q, int N, int D);
+// The key-chunk split (and so the workspace size) depends on the device's SM count.
+void decode_split(int B, int H, int n_q, int N, int D, int num_sms, int *splits, int *chunk);
+size_t decode_workspace_bytes(int B, int H, int n_q, int N, int D, int num_sms);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
 
 // Fixed scratch of fa_decode_noalloc (static device storage in decode.cu).
@@ -138,6 +138,12 @@ cudaError_t launch_bwd_dkdv_q128(const BwdArgs &a, const CUtensorMap &tq, const 
 cudaError_t launch_bwd_dkdv(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
                             const CUtensorMap &tv, const CUtensorMap &tdo, cudaStream_t s);
 cudaError_t launch_selftest_timeout(int *status, int limit_us, cudaStream_t s);
+
+// Head dimension a bf16 kernel is built for: the smallest of 64, 128, 192, 256 that holds D.  Any
+// D that is a multiple of 8 (so a row is a whole number of 16-byte units) runs on that kernel: the
+// TMA loads a 64-column panel that reaches past D with zeros, which add nothing to a score or an
+// output column, and the kernels store only the D real columns (row stride D).
+inline int kernel_head_dim(int D) { return D <= 64 ? 64 : D <= 128 ? 128 : D <= 192 ? 192 : 256; }
 
 inline int fwd_block_n(int D) {
     for (const auto &sp : kFwdSpecs)

@@ -351,7 +351,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float l_row = l + lsum[(g ^ 1) * kBM + r];
             tc_fence_after();
             const float inv_l = 1.f / l_row;
-            __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.o) + ((size_t)bh * N + row) * D + g * HD;
+            // row stride and stored columns: the caller's D (at most this kernel's D; the columns past it
+            // hold zeros from the TMA's out-of-bounds fill)
+            const int Dr = a.D;
+            __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.o) + ((size_t)bh * N + row) * Dr + g * HD;
             uint32_t ov[32];
 #pragma unroll
             for (int ch = 0; ch < HD / 32; ++ch) {
@@ -361,6 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + ch * 32);
 #pragma unroll
                     for (int v4 = 0; v4 < 4; ++v4) {
+                        if (g * HD + ch * 32 + v4 * 8 >= Dr) break;
                         uint4 w;
                         w.x = pack_bf16x2(__uint_as_float(ov[v4 * 8 + 0]) * inv_l, __uint_as_float(ov[v4 * 8 + 1]) * inv_l);
                         w.y = pack_bf16x2(__uint_as_float(ov[v4 * 8 + 2]) * inv_l, __uint_as_float(ov[v4 * 8 + 3]) * inv_l);
@@ -399,7 +403,7 @@ cudaError_t launch_spec(const FwdArgs &a, const CUtensorMap &tq, const CUtensorM
 
 cudaError_t launch_fwd_bf16(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             cudaStream_t s) {
-    switch (a.D) {
+    switch (kernel_head_dim(a.D)) {
         // measured choice per head dimension: the persistent two-tile kernel wherever its TMEM
         // layout fits (D <= 128; at D = 128 non-causal it measured equal to this kernel at
         // N = 4096 and 5-13 % faster at N = 1024, 2048 and 16384)

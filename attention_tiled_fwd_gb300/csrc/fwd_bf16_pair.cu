@@ -393,7 +393,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
             const float inv_l = 1.f / l;
-            __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.o) + ((size_t)w.bh * N + row) * D;
+            // row stride and stored columns: the caller's D (at most this kernel's D; the columns past it
+            // hold zeros from the TMA's out-of-bounds fill)
+            const int Dr = a.D;
+            __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.o) + ((size_t)w.bh * N + row) * Dr;
             uint32_t ov[32];
 #pragma unroll
             for (int ch = 0; ch < D / 32; ++ch) {
@@ -408,6 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + ch * 32);
 #pragma unroll
                     for (int v4 = 0; v4 < 4; ++v4) {
+                        if (ch * 32 + v4 * 8 >= Dr) break;
                         uint4 w4;
                         w4.x = pack_bf16x2(__uint_as_float(ov[v4 * 8 + 0]) * inv_l, __uint_as_float(ov[v4 * 8 + 1]) * inv_l);
                         w4.y = pack_bf16x2(__uint_as_float(ov[v4 * 8 + 2]) * inv_l, __uint_as_float(ov[v4 * 8 + 3]) * inv_l);
@@ -448,7 +452,7 @@ cudaError_t launch_spec(const FwdArgs &a, const CUtensorMap &tq, const CUtensorM
 
 cudaError_t launch_fwd_bf16_pair(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
                                  const CUtensorMap &tv, cudaStream_t s) {
-    switch (a.D) {
+    switch (kernel_head_dim(a.D)) {
         case 64: return launch_spec<64, 10>(a, tq, tk, tv, s);
         case 128: return launch_spec<128, 5>(a, tq, tk, tv, s);
         default: return cudaErrorInvalidValue;

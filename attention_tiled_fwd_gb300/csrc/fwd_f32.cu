@@ -12,6 +12,9 @@
 // shared memory (K rows padded by one float against bank conflicts).  Within
 // a tile, lane j scores key j for each of its warp's rows, the row max / sum
 // are warp reductions, and lane t owns output columns t, t+32, ...
+// Any D that is a multiple of 4 up to 256 runs: the staged tiles are D
+// rounded up to a multiple of 32 wide, the extra columns zero (they add
+// nothing to a score and their outputs are not stored).
 #include "fa_internal.h"
 #include <cfloat>
 #include <cmath>
@@ -35,13 +38,14 @@ __device__ __forceinline__ float warp_sum(float x) {
     return x;
 }
 
-template <int DPL>  // head dimension / 32 (columns per lane)
+template <int DPL>  // head dimension / 32, rounded up (columns per lane)
 __global__ void __launch_bounds__(kWarps * 32) fwd_f32_kernel(FwdArgs a) {
-    constexpr int D = DPL * 32;
+    constexpr int DP = DPL * 32;  // staged width
+    const int D = a.D;            // row stride and stored columns; D <= DP
     extern __shared__ float sm[];
-    float *q_s = sm;                      // [kBM][D]
-    float *k_s = q_s + kBM * D;           // [kBN][D + 1]
-    float *v_s = k_s + kBN * (D + 1);     // [kBN][D]
+    float *q_s = sm;                      // [kBM][DP]
+    float *k_s = q_s + kBM * DP;          // [kBN][DP + 1]
+    float *v_s = k_s + kBN * (DP + 1);    // [kBN][DP]
 
     int rank, bh;
     tile_order((a.N + kBM - 1) / kBM, a.B * a.H, a.causal, &rank, &bh);
@@ -53,9 +57,9 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_f32_kernel(FwdArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row0 = q_tile * kBM;
 
-    for (int idx = threadIdx.x; idx < kBM * D; idx += blockDim.x) {
-        int r = idx / D, c = idx % D;
-        q_s[idx] = (row0 + r < N) ? q[(size_t)(row0 + r) * D + c] : 0.f;
+    for (int idx = threadIdx.x; idx < kBM * DP; idx += blockDim.x) {
+        int r = idx / DP, c = idx % DP;
+        q_s[idx] = (row0 + r < N && c < D) ? q[(size_t)(row0 + r) * D + c] : 0.f;
     }
 
     float m[kRowsPerWarp], l[kRowsPerWarp], acc[kRowsPerWarp][DPL];
@@ -72,21 +76,21 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_f32_kernel(FwdArgs a) {
     for (int jt = 0; jt < n_tiles; ++jt) {
         const int key0 = jt * kBN;
         __syncthreads();  // previous tile fully consumed (and q_s written on the first pass)
-        for (int idx = threadIdx.x; idx < kBN * D; idx += blockDim.x) {
-            int r = idx / D, c = idx % D;
-            bool ok = key0 + r < N;
-            k_s[r * (D + 1) + c] = ok ? k[(size_t)(key0 + r) * D + c] : 0.f;
-            v_s[r * D + c] = ok ? v[(size_t)(key0 + r) * D + c] : 0.f;
+        for (int idx = threadIdx.x; idx < kBN * DP; idx += blockDim.x) {
+            int r = idx / DP, c = idx % DP;
+            bool ok = key0 + r < N && c < D;
+            k_s[r * (DP + 1) + c] = ok ? k[(size_t)(key0 + r) * D + c] : 0.f;
+            v_s[r * DP + c] = ok ? v[(size_t)(key0 + r) * D + c] : 0.f;
         }
         __syncthreads();
         const int key = key0 + lane;
 #pragma unroll
         for (int r = 0; r < kRowsPerWarp; ++r) {
             const int row = row0 + warp * kRowsPerWarp + r;
-            const float *qr = q_s + (warp * kRowsPerWarp + r) * D;
+            const float *qr = q_s + (warp * kRowsPerWarp + r) * DP;
             float s = 0.f;
 #pragma unroll 8
-            for (int d = 0; d < D; ++d) s = fmaf(qr[d], k_s[lane * (D + 1) + d], s);
+            for (int d = 0; d < DP; ++d) s = fmaf(qr[d], k_s[lane * (DP + 1) + d], s);
             s *= a.scale_log2;  // base-2 domain
             if (key >= N || (a.causal && key > row)) s = -INFINITY;
             const float m_new = fmaxf(m[r], warp_max(s));
@@ -101,7 +105,7 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_f32_kernel(FwdArgs a) {
             for (int j = 0; j < kBN; ++j) {
                 const float pj = __shfl_sync(0xffffffffu, p, j);
 #pragma unroll
-                for (int t = 0; t < DPL; ++t) acc[r][t] = fmaf(pj, v_s[j * D + t * 32 + lane], acc[r][t]);
+                for (int t = 0; t < DPL; ++t) acc[r][t] = fmaf(pj, v_s[j * DP + t * 32 + lane], acc[r][t]);
             }
         }
     }
@@ -113,15 +117,16 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_f32_kernel(FwdArgs a) {
         if (row >= N) continue;
         const float inv = 1.f / l[r];
 #pragma unroll
-        for (int t = 0; t < DPL; ++t) o[(size_t)row * D + t * 32 + lane] = acc[r][t] * inv;
+        for (int t = 0; t < DPL; ++t)
+            if (t * 32 + lane < D) o[(size_t)row * D + t * 32 + lane] = acc[r][t] * inv;
         if (lane == 0) a.lse[(size_t)bh * N + row] = (m[r] + log2f(l[r])) * 0.69314718055994531f;
     }
 }
 
 template <int DPL>
 cudaError_t launch_dpl(const FwdArgs &a, cudaStream_t s) {
-    constexpr int D = DPL * 32;
-    const size_t smem = sizeof(float) * (size_t)(kBM * D + kBN * (D + 1) + kBN * D);
+    constexpr int DP = DPL * 32;
+    const size_t smem = sizeof(float) * (size_t)(kBM * DP + kBN * (DP + 1) + kBN * DP);
     cudaError_t e = cudaFuncSetAttribute(fwd_f32_kernel<DPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
@@ -133,7 +138,7 @@ cudaError_t launch_dpl(const FwdArgs &a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_fwd_f32(const FwdArgs &a, cudaStream_t s) {
-    switch (a.D / 32) {
+    switch ((a.D + 31) / 32) {
         case 1: return launch_dpl<1>(a, s);
         case 2: return launch_dpl<2>(a, s);
         case 3: return launch_dpl<3>(a, s);

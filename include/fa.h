@@ -75,9 +75,19 @@ enum fa_status {
 /*
  * fa_forward -- O = softmax(scale Q K^T) V and LSE (natural log-sum-exp of the
  * scaled scores of each row).
- *   dtype FA_BF16: D in {64, 128, 192, 256}; bf16 inputs, fp32 accumulation
- *                  (tcgen05 tensor cores), bf16 O, fp32 LSE.
- *   dtype FA_F32 : D a multiple of 32 in [32, 256]; fp32 inputs and O,
+ *   Defined by: "Learning Metal with FlashAttention", section "FlashAttention"
+ *   (the attention definition and its streaming form: running max m, running
+ *   sum l, O rescaled per K/V tile and divided by l after the last one); the
+ *   forward pseudocode of "FlashAttention (Metal port)" (metal-flash-
+ *   attention), performance section (L = m + log l written out); tiles above
+ *   the causal diagonal skipped, exponent in base 2: "Flash Attention"
+ *   (metalworking), kernel anatomy items 1-4.
+ *   dtype FA_BF16: D a multiple of 8 in [8, 256]; bf16 inputs, fp32
+ *                  accumulation (tcgen05 tensor cores), bf16 O, fp32 LSE.
+ *                  Kernels exist for D = 64, 128, 192, 256; any other D runs
+ *                  on the next wider one with the extra columns read as
+ *                  zeros (the rows keep the caller's stride D).
+ *   dtype FA_F32 : D a multiple of 4 in [4, 256]; fp32 inputs and O,
  *                  fp32 FFMA arithmetic throughout, fp32 LSE.
  *   N >= 1 arbitrary (ragged tails are masked).  causal: 0 or non-zero.
  */
@@ -87,11 +97,16 @@ FA_API int fa_forward(const void *q, const void *k, const void *v, void *o, floa
 
 /*
  * fa_backward_dq -- first half of the split backward ("backward query"):
+ *   Defined by: "FlashAttention (Metal port)" (metal-flash-attention), the
+ *   backward-query pseudocode of its performance section (D = dO * O read as
+ *   the row sum; P = exp(S - L) with S the scaled scores), and its
+ *   documentation section (dQ and dK/dV as two kernels, 7 GEMMs, no atomics).
  *   delta_i = sum_d dO_id O_id            (written: delta [B,H,N] fp32)
  *   P = exp(S - LSE), dP = dO V^T, dS = P * (dP - delta) * scale,
  *   dQ = dS K                              (written: dq, grad_dtype)
  * o and lse are the outputs of fa_forward on the same q, k, v, scale, causal.
- * Supported: dtype FA_BF16 with D in {64, 128}; grad_dtype FA_F32 or FA_BF16.
+ * Supported: dtype FA_BF16 with D a multiple of 8 in [8, 256] (as for
+ * fa_forward); grad_dtype FA_F32 or FA_BF16.
  */
 FA_API int fa_backward_dq(const void *q, const void *k, const void *v, const void *o,
                    const void *dO, const float *lse, float *delta, void *dq,
@@ -101,11 +116,15 @@ FA_API int fa_backward_dq(const void *q, const void *k, const void *v, const voi
 /*
  * fa_backward_dkdv -- second half ("backward key-value"), one CTA per K/V
  * tile iterating over query tiles:
+ *   Defined by: "FlashAttention (Metal port)" (metal-flash-attention), the
+ *   backward-key-value pseudocode of its performance section (delta and L of
+ *   every query row read; dS^T carries the softmax scale).
  *   P^T = exp(S^T - LSE), dV = P^T dO, dP^T = V dO^T,
  *   dS^T = P^T * (dP^T - delta) * scale, dK = dS^T Q
  * lse from fa_forward, delta from fa_backward_dq (enqueue this call after it
  * on the same stream, or order the two streams yourself).
- * Supported: dtype FA_BF16 with D in {64, 128}; grad_dtype FA_F32 or FA_BF16.
+ * Supported: dtype FA_BF16 with D a multiple of 8 in [8, 256] (as for
+ * fa_forward); grad_dtype FA_F32 or FA_BF16.
  */
 FA_API int fa_backward_dkdv(const void *q, const void *k, const void *v, const void *dO,
                      const float *lse, const float *delta, void *dk, void *dv,
@@ -156,7 +175,10 @@ FA_API int fa_decode(const void *q, const void *k, const void *v, void *o, float
                      int B, int H, int n_q, int N, int D, float scale, int causal,
                      void *workspace, size_t workspace_bytes, void *stream);
 
-/* Bytes of workspace fa_decode needs for these sizes (written to *bytes). */
+/* Bytes of workspace fa_decode needs for these sizes (written to *bytes).  The
+ * key range is split for the current device's SM count, so the answer is for
+ * the device that is current at this call (the GB300's 152 SMs if no device
+ * can be queried); call fa_decode on that same device. */
 FA_API int fa_decode_workspace_bytes(int B, int H, int n_q, int N, int D, size_t *bytes);
 
 /* Size of the fixed per-device scratch that fa_decode_noalloc works in. */

@@ -21,7 +21,8 @@ FlashAttention" ("Benchmark" section) is shape-compatible with
 ``fwd_bf16_b4h16n2048d128`` (same N and D); the 32K-context case of the
 metalworking "Flash Attention" page is ``fwdbwd_bf16_b1h32n32768d64_causal``;
 the large-head-dimension (D=256) register-pressure case of the
-metal-flash-attention page is ``fwd_bf16_b1h8n8192d256``.  No public dataset
+metal-flash-attention page is ``fwd_bf16_b1h8n8192d256`` (forward) and
+``fwdbwd_bf16_b1h8n8192d256`` (forward and backward).  No public dataset
 is involved: attention inputs are i.i.d. Gaussian.
 """
 from __future__ import annotations
@@ -60,6 +61,9 @@ WORKLOADS: Dict[str, Workload] = {
         Workload("bwd_bf16_b2h16n4096d128_causal", 2, 16, 4096, 128, "bf16", (True,), ("fwd", "bwd"), 1004,
                  grad_dtypes=("f32", "bf16")),
         Workload("fwdbwd_bf16_b1h32n32768d64_causal", 1, 32, 32768, 64, "bf16", (True,), ("fwd", "bwd"), 1005,
+                 grad_dtypes=("bf16",)),
+        # the D = 256 shape above with a backward as well (the wide-head backward kernels)
+        Workload("fwdbwd_bf16_b1h8n8192d256", 1, 8, 8192, 256, "bf16", (False,), ("fwd", "bwd"), 1006, std=0.5,
                  grad_dtypes=("bf16",)),
     )
 }

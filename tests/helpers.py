@@ -31,12 +31,34 @@ def to_np(t: torch.Tensor) -> np.ndarray:
     return t.detach().to("cpu").double().numpy()
 
 
+# Every comparison's raw max-abs error, with the flat bound it is measured against, so that a run
+# can show how close the errors come to the flat bounds and whether the bf16 rounding allowance
+# (rel > 0) was ever needed.  conftest.py prints a summary and can write it out as JSON.
+ERROR_LOG = []
+
+
+def assert_scaled(got, ref, frac: float, what: str = ""):
+    """max |err| <= frac * max |ref|: for outputs whose magnitude is far below the flat bound (the D = 256
+    workloads draw inputs with std 0.5, so O and the gradients there are ~0.02 and an all-zero result
+    would pass 2e-2 on its own), the error must also be small against the output's own scale."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    err = float(np.abs(got - ref).max())
+    scale = float(np.abs(ref).max())
+    assert scale > 0 and err <= frac * scale, f"{what}: max |err| {err:.3e} > {frac} x max |ref| {scale:.3e}"
+    return err / scale
+
+
 def assert_close(got, ref, atol: float, rel: float = 0.0, what: str = ""):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, (what, got.shape, ref.shape)
     assert np.isfinite(got).all(), f"{what}: non-finite values"
     err = np.abs(got - ref)
+    if err.size:
+        ERROR_LOG.append({"what": what, "max_abs_err": float(err.max()), "max_abs_ref": float(np.abs(ref).max()),
+                          "flat_bound": float(atol), "rel": float(rel),
+                          "flat_bound_held": bool(err.max() <= atol)})
     bound = atol + rel * np.abs(ref)
     worst = float((err - bound).max()) if err.size else -1.0
     if worst > 0:

@@ -17,7 +17,8 @@ def test_wrapper_is_exported():
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("shape,causal", [((1, 2, 200, 64), True), ((2, 1, 333, 128), False),
-                                          ((1, 1, 257, 128), True)])
+                                          ((1, 1, 257, 128), True), ((1, 1, 150, 96), True),
+                                          ((1, 1, 140, 256), False), ((1, 2, 99, 192), True)])
 def test_autograd_matches_oracle(shape, causal):
     import attention_tiled_fwd_gb300 as fa
     dev = cuda_or_skip()

@@ -33,9 +33,13 @@ def test_forward_rejects_bad_shapes(lib):
 
 
 def test_forward_rejects_head_dims(lib):
-    for D in (0, 16, 32, 96, 100, 160, 320, 512):
+    # bf16: any multiple of 8 up to 256
+    for D in (0, 4, 12, 100, 252, 260, 264, 320, 512):
         assert fwd(lib, D=D) in (nat.FA_ERR_HEAD_DIM, nat.FA_ERR_SHAPE), D
-    for D in (48, 100, 288):
+    for D in (8, 16, 32, 96, 160, 200, 256):
+        assert fwd(lib, D=D) not in (nat.FA_ERR_HEAD_DIM, nat.FA_ERR_SHAPE), D
+    # fp32: any multiple of 4 up to 256
+    for D in (2, 6, 50, 258, 260, 288):
         assert fwd(lib, D=D, dtype=nat.FA_F32) == nat.FA_ERR_HEAD_DIM, D
 
 
@@ -65,14 +69,17 @@ def test_backward_rejects(lib):
                                     a["B"], a["H"], a["N"], a["D"], a["scale"], a["causal"], a["dtype"],
                                     a["grad"], None)
 
-    assert dq(D=256) == nat.FA_ERR_HEAD_DIM
-    assert dq(D=32) == nat.FA_ERR_HEAD_DIM
+    assert dq(D=264) == nat.FA_ERR_HEAD_DIM
+    assert dq(D=36) == nat.FA_ERR_HEAD_DIM
+    assert dq(D=256) != nat.FA_ERR_HEAD_DIM and dq(D=40) != nat.FA_ERR_HEAD_DIM
     assert dq(grad=5) == nat.FA_ERR_DTYPE
     assert dq(dtype=nat.FA_F32) == nat.FA_ERR_DTYPE
     assert dq(delta=None) == nat.FA_ERR_NULL
     assert dq(dO=A + 4) == nat.FA_ERR_ALIGN
     assert dq(N=0) == nat.FA_ERR_SHAPE
-    assert dkdv(D=256) == nat.FA_ERR_HEAD_DIM
+    assert dkdv(D=288) == nat.FA_ERR_HEAD_DIM
+    assert dkdv(D=20) == nat.FA_ERR_HEAD_DIM
+    assert dkdv(D=192) != nat.FA_ERR_HEAD_DIM
     assert dkdv(dv=None) == nat.FA_ERR_NULL
     assert dkdv(scale=float("inf")) == nat.FA_ERR_SCALE
     assert dkdv(lse=A + 12) == nat.FA_ERR_ALIGN
