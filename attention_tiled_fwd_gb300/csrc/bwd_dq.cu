@@ -20,10 +20,10 @@
 // half (32 keys) of every tile's columns -- dS is elementwise given the row's
 // L and D, so the halves never exchange data, and two warps per SM
 // sub-partition hide each other's latencies (four warpgroups of 16 keys
-// measured 3 % slower here).  The compute warps compute D while Q and dO are
-// loading, each warpgroup over its own share of the row: D over the whole row
-// per thread outlasted the load and delayed the first products, by ~12 % of
-// the kernel's time at N = 4096; D after the Q copy delayed the first dS.
+// measured 3 % slower here).  The producer stages O's tile beside Q and dO
+// (TMA), and each warpgroup sums its share of D_i = rowsum(dO * O) from the two
+// shared tiles; reading O and dO rows from global memory took ~4 us per CTA,
+// a third of a CTA's fixed cost.
 // TMEM (128 lanes = queries): S[b] = [64b, 64b+64), dP[b] = [128+64b, ...),
 // dQ [256, 256+D), b = j % 2, dS[b] = [256+D+32b, +32), then Q as bf16
 // pairs.  This kernel serves D = 128 (D = 64 runs bwd_dq_k128.cu, whose
@@ -67,15 +67,21 @@ enum : int { kSiteQ = 21, kSiteSlotEmpty, kSiteSlotFull, kSiteSFull, kSiteDsFull
 
 template <int D, int NSLOT>
 struct DqSmem {
-    static constexpr int kQBytes = kBM * D * 2;     // Q and dO: 128 x D bf16 each
+    static constexpr int kQBytes = kBM * D * 2;     // Q, dO and O: 128 x D bf16 each
     static constexpr int kTileBytes = kBN * D * 2;  // one K_j or V_j tile
     static constexpr int kQOff = 0;
     static constexpr int kDoOff = kQBytes;
     static constexpr int kSlotOff = 2 * kQBytes;
-    static constexpr int kDeltaOff = kSlotOff + NSLOT * kTileBytes;  // [kComputeWG][kBM] partial sums of dO * O
+    static constexpr int kOOff = kSlotOff + NSLOT * kTileBytes;
+    // q_full, slot_full[NSLOT], slot_empty[NSLOT], s_full[2], ds_full[2], final, a_final, dq_done[2], qt_ready,
+    // o_full
+    static constexpr int kNumBars = 1 + 2 * NSLOT + 10;
+    static constexpr int kRest = kComputeWG * kBM * 4 + kNumBars * 8 + 16 + 1024;
+    // O's tile is staged by TMA where it fits (D = 128): D_i is then summed from shared memory.  At larger D
+    // the compute warps read the O and dO rows from global memory instead.
+    static constexpr bool kOTile = kOOff + kQBytes + kRest <= 232448;
+    static constexpr int kDeltaOff = kOOff + (kOTile ? kQBytes : 0);  // [kComputeWG][kBM] partial sums
     static constexpr int kBarOff = kDeltaOff + kComputeWG * kBM * 4;
-    // q_full, slot_full[NSLOT], slot_empty[NSLOT], s_full[2], ds_full[2], final, a_final, dq_done[2], qt_ready
-    static constexpr int kNumBars = 1 + 2 * NSLOT + 9;
     static constexpr int kTmemHolderOff = kBarOff + kNumBars * 8;
     static constexpr int kAlloc = kTmemHolderOff + 16 + 1024;
 };
@@ -87,7 +93,7 @@ template <int D, int DQ, bool QT, int NSLOT>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
-                  BwdArgs a) {
+                  const __grid_constant__ CUtensorMap tmap_o, BwdArgs a) {
     using L = DqSmem<D, NSLOT>;
     constexpr int kPanels = D / 64;
     constexpr uint32_t kTmemCols = 512;
@@ -100,6 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *q_s = smem + L::kQOff;
     uint8_t *do_s = smem + L::kDoOff;
     uint8_t *slots = smem + L::kSlotOff;
+    uint8_t *o_s = smem + L::kOOff;  // O's tile (kOTile only)
     float *delta_s = reinterpret_cast<float *>(smem + L::kDeltaOff);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
     uint64_t *q_full = bars;
@@ -111,6 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *a_final = final_bar + 1;  // issuer A: every S / dP MMA has completed
     uint64_t *dq_done = a_final + 1;    // [2]: dQ_j completed (its dS buffer j % 2 is free)
     uint64_t *qt_ready = dq_done + 2;   // Q is in TMEM
+    uint64_t *o_full = qt_ready + 1;    // O's tile landed (kOTile)
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kTmemHolderOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -137,6 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(a_final, 1);
         for (int b = 0; b < 2; ++b) mbar_init(&dq_done[b], 1);
         mbar_init(qt_ready, 4 * kComputeWG);  // one arrive per compute warp
+        mbar_init(o_full, 1);
         fence_mbarrier_init();
     }
     if (warp == 1) {
@@ -160,6 +169,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_3d(q_s + p * (kBM * 128), &tmap_q, q_full, p * 64, q_tile * kBM, bh);
                 tma_load_3d(do_s + p * (kBM * 128), &tmap_do, q_full, p * 64, q_tile * kBM, bh);
             }
+            if constexpr (L::kOTile) {
+                tma_prefetch_desc(&tmap_o);
+                mbar_arrive_expect_tx(o_full, L::kQBytes);
+#pragma unroll
+                for (int p = 0; p < kPanels; ++p)
+                    tma_load_3d(o_s + p * (kBM * 128), &tmap_o, o_full, p * 64, q_tile * kBM, bh);
+            }
             int last_round[NSLOT];
 #pragma unroll
             for (int s = 0; s < NSLOT; ++s) last_round[s] = -1;
@@ -180,6 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < NSLOT; ++s)
                 if (last_round[s] >= 0) mbar_wait(&slot_full[s], last_round[s] & 1, a.status, kSiteDrain);
             mbar_wait(q_full, 0, a.status, kSiteDrain);
+            if constexpr (L::kOTile) mbar_wait(o_full, 0, a.status, kSiteDrain);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -263,12 +280,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float c = a.scale_log2;
         // P = 2^(S c - L log2 e); invalid rows get P = 0.
         const float lse2 = valid ? a.lse[(size_t)bh * N + row] * 1.4426950408889634f : INFINITY;
-        // D_i = sum_d dO_id O_id for this thread's row, while the producer's TMA brings in Q and dO (nothing
-        // can start before they land): warpgroup g sums columns [g D / kComputeWG, (g + 1) D / kComputeWG),
-        // the partial sums meet in shared memory, and every warpgroup adds them in the same order.
+        // D_i = sum_d dO_id O_id for this thread's row: warpgroup g sums columns [g D / kComputeWG,
+        // (g + 1) D / kComputeWG), the partial sums meet in shared memory, and every warpgroup adds them in
+        // the same order.  With O's tile staged, both operands come from the swizzled shared tiles, whose
+        // chunk k of row r sits at the same place in each (columns past the caller's D and rows past N are
+        // zeros from the TMA); otherwise from the rows in global memory.
         constexpr int kDCols = D / kComputeWG;
         float delta = 0.f;
-        if (valid) {
+        if constexpr (L::kOTile) {
+            bool ook = mbar_wait(o_full, 0, a.status, kSiteQ) && mbar_wait(q_full, 0, a.status, kSiteQ);
+            if (__all_sync(0xffffffffu, ook)) {
+#pragma unroll
+                for (int p = g * (kDCols / 64); p < (g + 1) * (kDCols / 64); ++p) {
+                    const uint8_t *orow = o_s + p * (kBM * 128) + r * 128;
+                    const uint8_t *drow = do_s + p * (kBM * 128) + r * 128;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        // the swizzled position of chunk k: lanes (rows) spread over all 32 banks
+                        const uint4 ov = *reinterpret_cast<const uint4 *>(orow + ((k ^ (r & 7)) << 4));
+                        const uint4 dv = *reinterpret_cast<const uint4 *>(drow + ((k ^ (r & 7)) << 4));
+                        const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, dw[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ow[t]));
+                            const float2 df = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&dw[t]));
+                            delta = fmaf(of.x, df.x, delta);
+                            delta = fmaf(of.y, df.y, delta);
+                        }
+                    }
+                }
+            }
+        } else if (valid) {
             const uint4 *orow = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.o) +
                                                                 ((size_t)bh * N + row) * Dr + g * kDCols);
             const uint4 *drow = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.dO) +
@@ -294,9 +336,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int t = 0; t < kComputeWG; ++t) delta += delta_s[t * kBM + r];
         if (valid && g == 0 && blockIdx.y == 0) a.delta[(size_t)bh * N + row] = delta;
-        const int lim = a.causal ? min(N - 1, row) : N - 1;  // last visible key
-        // Q rows into TMEM as bf16 pairs, one 64-column panel per warpgroup
-        // (row r of a panel is 128 B at r * 128, its 16-byte chunk k stored at k ^ (r % 8))
+        // Q rows into TMEM as bf16 pairs, one 64-column panel per warpgroup (row r of a panel is 128 B at
+        // r * 128, its 16-byte chunk k stored at k ^ (r % 8)).  Copying Q before summing D_i lets S_0 and dP_0
+        // start earlier but measured 6 % slower per key tile over long rows, so D_i comes first.
         {
             bool qok = !QT || mbar_wait(q_full, 0, a.status, kSiteQ);
             if (!__all_sync(0xffffffffu, qok)) qok = false;
@@ -320,6 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             warp_arrive(qt_ready);
         }
+        const int lim = a.causal ? min(N - 1, row) : N - 1;  // last visible key
         constexpr int kHalf = kBN / kComputeWG;              // columns per thread per tile
         const uint64_t c2 = f2_pack(c, c), nl2 = f2_pack(-lse2, -lse2), d2 = f2_pack(delta, delta);
         bool ok = true;
@@ -412,25 +455,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, int DQ, bool QT, int NSLOT>
 cudaError_t launch_spec(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                        const CUtensorMap &tdo, cudaStream_t s) {
+                        const CUtensorMap &tdo, const CUtensorMap &to, cudaStream_t s) {
     using L = DqSmem<D, NSLOT>;
     static_assert(L::kAlloc <= 232448, "shared memory budget");
     auto kern = bwd_dq_kernel<D, DQ, QT, NSLOT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     dim3 grid(((a.N + kBM - 1) / kBM) * a.H * a.B, D / DQ);
-    kern<<<grid, kThreads, L::kAlloc, s>>>(tq, tk, tv, tdo, a);
+    kern<<<grid, kThreads, L::kAlloc, s>>>(tq, tk, tv, tdo, to, a);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_dq(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                          const CUtensorMap &tdo, cudaStream_t s) {
+                          const CUtensorMap &tdo, const CUtensorMap &to, cudaStream_t s) {
     switch (kernel_head_dim(a.D)) {
-        case 128: return launch_spec<128, 128, true, 8>(a, tq, tk, tv, tdo, s);
-        case 192: return launch_spec<192, 192, false, 5>(a, tq, tk, tv, tdo, s);
-        case 256: return launch_spec<256, 128, false, 3>(a, tq, tk, tv, tdo, s);
+        case 128: return launch_spec<128, 128, true, 8>(a, tq, tk, tv, tdo, to, s);
+        case 192: return launch_spec<192, 192, false, 5>(a, tq, tk, tv, tdo, to, s);
+        case 256: return launch_spec<256, 128, false, 3>(a, tq, tk, tv, tdo, to, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -56,11 +56,12 @@ struct K128Smem {
     static constexpr int kQOff = 0;
     static constexpr int kDoOff = kQBytes;
     static constexpr int kSlotOff = 2 * kQBytes;
-    static constexpr int kDeltaOff = kSlotOff + kNSlot * kTileBytes;  // [kComputeWG][kBM] partial sums of dO * O
+    static constexpr int kOOff = kSlotOff + kNSlot * kTileBytes;  // O's tile (for D_i)
+    static constexpr int kDeltaOff = kOOff + kQBytes;  // [kComputeWG][kBM] partial sums of dO * O
     static constexpr int kBarOff = kDeltaOff + kComputeWG * kBM * 4;
     // q_full, slot_full[kNSlot], slot_empty[kNSlot], s_full, s_free, ds_full[2], dq_done[2], dp_full, dp_free,
-    // qt_ready, final, a_final
-    static constexpr int kNumBars = 1 + 2 * kNSlot + 2 + 4 + 2 + 3;
+    // qt_ready, final, a_final, o_full
+    static constexpr int kNumBars = 1 + 2 * kNSlot + 2 + 4 + 2 + 4;
     static constexpr int kTmemHolderOff = kBarOff + kNumBars * 8;
     static constexpr int kAlloc = kTmemHolderOff + 16 + 1024;
 };
@@ -68,7 +69,7 @@ struct K128Smem {
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_k128_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                        const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
-                       BwdArgs a) {
+                       const __grid_constant__ CUtensorMap tmap_o, BwdArgs a) {
     using L = K128Smem;
     constexpr uint32_t kTmemCols = 512;
     // TMEM columns: S = [0, 128) and dP = [128, 256), each single-buffered and released as soon as every
@@ -82,6 +83,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *q_s = smem + L::kQOff;
     uint8_t *do_s = smem + L::kDoOff;
+    uint8_t *o_s = smem + L::kOOff;
     uint8_t *slots = smem + L::kSlotOff;
     float *delta_s = reinterpret_cast<float *>(smem + L::kDeltaOff);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
@@ -97,6 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *qt_ready = dp_free + 1;        // Q and dO are in TMEM
     uint64_t *final_bar = qt_ready + 1;      // issuer B: every dQ MMA has completed
     uint64_t *a_final = final_bar + 1;       // issuer A: every S / dP MMA has completed
+    uint64_t *o_full = a_final + 1;          // O's tile landed
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kTmemHolderOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -124,6 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(qt_ready, kComputeWarps);
         mbar_init(final_bar, 1);
         mbar_init(a_final, 1);
+        mbar_init(o_full, 1);
         fence_mbarrier_init();
     }
     if (warp == 1) {
@@ -144,6 +148,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(q_full, 2 * L::kQBytes);
             tma_load_3d(q_s, &tmap_q, q_full, 0, q_tile * kBM, bh);
             tma_load_3d(do_s, &tmap_do, q_full, 0, q_tile * kBM, bh);
+            tma_prefetch_desc(&tmap_o);
+            mbar_arrive_expect_tx(o_full, L::kQBytes);
+            tma_load_3d(o_s, &tmap_o, o_full, 0, q_tile * kBM, bh);
             int last_round[kNSlot];
 #pragma unroll
             for (int s = 0; s < kNSlot; ++s) last_round[s] = -1;
@@ -162,6 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < kNSlot; ++s)
                 if (last_round[s] >= 0) mbar_wait(&slot_full[s], last_round[s] & 1, a.status, kSiteDrain);
             mbar_wait(q_full, 0, a.status, kSiteDrain);
+            mbar_wait(o_full, 0, a.status, kSiteDrain);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -240,41 +248,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float c = a.scale_log2;
         // P = 2^(S c - L log2 e); invalid rows get P = 0.
         const float lse2 = valid ? a.lse[(size_t)bh * N + row] * 1.4426950408889634f : INFINITY;
-        // D_i = sum_d dO_id O_id for this thread's row, while the producer's TMA brings in Q and dO:
-        // warpgroup g sums columns [16g, 16g + 16); the partial sums meet in shared memory and every
-        // warpgroup adds them in the same order.
         // Row stride and real columns: the caller's D (a multiple of 8, at most 64; TMA fills the rest of
         // the 64-column panels with zeros, which add nothing).
         const int Dr = a.D;
-        float delta = 0.f;
-        if (valid) {
-            const uint4 *orow = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.o) +
-                                                                ((size_t)bh * N + row) * Dr + 16 * g);
-            const uint4 *drow = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.dO) +
-                                                                ((size_t)bh * N + row) * Dr + 16 * g);
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                if (16 * g + 8 * i >= Dr) break;
-                const uint4 ov = orow[i], dv = drow[i];
-                const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, dw[4] = {dv.x, dv.y, dv.z, dv.w};
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ow[t]));
-                    const float2 df = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&dw[t]));
-                    delta = fmaf(of.x, df.x, delta);
-                    delta = fmaf(of.y, df.y, delta);
-                }
-            }
-        }
-        delta_s[g * kBM + r] = delta;
-        // every compute warp reaches this barrier: nothing before it waits or exits early
-        asm volatile("bar.sync 1, %0;" ::"r"(128 * kComputeWG) : "memory");
-        delta = 0.f;
-#pragma unroll
-        for (int t = 0; t < kComputeWG; ++t) delta += delta_s[t * kBM + r];
-        if (valid && g == 0) a.delta[(size_t)bh * N + row] = delta;
-        // Q (warpgroup 0) and dO (warpgroup 1) rows into TMEM as bf16 pairs (row r of the 64-column panel is
-        // 128 B at r * 128, its 16-byte chunk k stored at k ^ (r % 8))
+        // Q (warpgroup 0) and dO (warpgroup 1) rows into TMEM as bf16 pairs first thing, so that S_0 and dP_0
+        // run while D_i is summed (row r of the 64-column panel is 128 B at r * 128, its 16-byte chunk k
+        // stored at k ^ (r % 8))
         {
             bool qok = mbar_wait(q_full, 0, a.status, kSiteQ);
             if (!__all_sync(0xffffffffu, qok)) qok = false;
@@ -295,6 +274,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             warp_arrive(qt_ready);
         }
+        // D_i = sum_d dO_id O_id for this thread's row, from the staged O and dO tiles (both swizzled alike, so
+        // chunk k of row r sits at the same place in each; columns past the caller's D and rows past N are
+        // zeros from the TMA): warpgroup g sums columns [16g, 16g + 16); the partial sums meet in shared
+        // memory and every warpgroup adds them in the same order.
+        float delta = 0.f;
+        {
+            const bool ook = mbar_wait(o_full, 0, a.status, kSiteQ);
+            if (__all_sync(0xffffffffu, ook)) {
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int off = r * 128 + (((2 * g + i) ^ (r & 7)) << 4);
+                    const uint4 ov = *reinterpret_cast<const uint4 *>(o_s + off);
+                    const uint4 dv = *reinterpret_cast<const uint4 *>(do_s + off);
+                    const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, dw[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ow[t]));
+                        const float2 df = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&dw[t]));
+                        delta = fmaf(of.x, df.x, delta);
+                        delta = fmaf(of.y, df.y, delta);
+                    }
+                }
+            }
+        }
+        delta_s[g * kBM + r] = delta;
+        // every compute warp reaches this barrier: nothing before it waits or exits early
+        asm volatile("bar.sync 1, %0;" ::"r"(128 * kComputeWG) : "memory");
+        delta = 0.f;
+#pragma unroll
+        for (int t = 0; t < kComputeWG; ++t) delta += delta_s[t * kBM + r];
+        if (valid && g == 0) a.delta[(size_t)bh * N + row] = delta;
         const int lim = a.causal ? min(N - 1, row) : N - 1;  // last visible key
         const uint64_t c2 = f2_pack(c, c), nl2 = f2_pack(-lse2, -lse2), d2 = f2_pack(delta, delta);
         bool ok = true;
@@ -393,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_bwd_dq_k128(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                               const CUtensorMap &tdo, cudaStream_t s) {
+                               const CUtensorMap &tdo, const CUtensorMap &to, cudaStream_t s) {
     using L = K128Smem;
     static_assert(L::kAlloc <= 232448, "shared memory budget");
     if (kernel_head_dim(a.D) != kD) return cudaErrorInvalidValue;
@@ -401,7 +411,7 @@ cudaError_t launch_bwd_dq_k128(const BwdArgs &a, const CUtensorMap &tq, const CU
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     dim3 grid(((a.N + kBM - 1) / kBM) * a.H * a.B);
-    kern<<<grid, kThreads, L::kAlloc, s>>>(tq, tk, tv, tdo, a);
+    kern<<<grid, kThreads, L::kAlloc, s>>>(tq, tk, tv, tdo, to, a);
     return cudaGetLastError();
 }
 

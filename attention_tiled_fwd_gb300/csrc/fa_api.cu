@@ -193,17 +193,17 @@ extern "C" int fa_backward_dq(const void *q, const void *k, const void *v, const
     if (rc != FA_OK) return rc;
     BwdArgs a{q, k, v, o, dO, lse, delta, dq, nullptr, nullptr, B, H, N, D, scale, scale * log2e(),
               causal ? 1 : 0, grad_dtype == FA_BF16 ? 1 : 0, st->status_word};
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, to;
     // D <= 64 runs the 128-key-tile kernel (its score products are N = 128 MMAs); wider heads the 64-key one
     const int Dk = kernel_head_dim(D);
     const int kv_rows = Dk == 64 ? 128 : kDqKRows;
     if (encode_bf16_3d(&tq, q, B * H, N, D, 128) != FA_OK ||
         encode_bf16_3d(&tk, k, B * H, N, D, kv_rows) != FA_OK ||
         encode_bf16_3d(&tv, v, B * H, N, D, kv_rows) != FA_OK ||
-        encode_bf16_3d(&tdo, dO, B * H, N, D, 128) != FA_OK)
+        encode_bf16_3d(&tdo, dO, B * H, N, D, 128) != FA_OK || encode_bf16_3d(&to, o, B * H, N, D, 128) != FA_OK)
         return FA_ERR_CUDA;
-    cudaError_t e = Dk == 64 ? launch_bwd_dq_k128(a, tq, tk, tv, tdo, reinterpret_cast<cudaStream_t>(stream))
-                             : launch_bwd_dq(a, tq, tk, tv, tdo, reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e = Dk == 64 ? launch_bwd_dq_k128(a, tq, tk, tv, tdo, to, reinterpret_cast<cudaStream_t>(stream))
+                             : launch_bwd_dq(a, tq, tk, tv, tdo, to, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
