@@ -93,7 +93,8 @@ template <int D, int DQ, bool QT, int NSLOT>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
-                  const __grid_constant__ CUtensorMap tmap_o, BwdArgs a) {
+                  const __grid_constant__ CUtensorMap tmap_o, const __grid_constant__ CUtensorMap tmap_dq,
+                  BwdArgs a) {
     using L = DqSmem<D, NSLOT>;
     constexpr int kPanels = D / 64;
     constexpr uint32_t kTmemCols = 512;
@@ -121,6 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *o_full = qt_ready + 1;    // O's tile landed (kOTile)
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kTmemHolderOff);
 
+    __shared__ int epi_abort;  // a compute warp's wait ran out: the epilogue stores nothing
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int rank, bh;
     tile_order((a.N + kBM - 1) / kBM, a.B * a.H, a.causal, &rank, &bh);
@@ -132,6 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int Dr = a.D;                         // row stride and real columns (<= D; the rest are zeros)
 
     if (threadIdx.x == 0) {
+        epi_abort = 0;
         mbar_init(q_full, 1);
         for (int s = 0; s < NSLOT; ++s) {
             mbar_init(&slot_full[s], 1);
@@ -406,42 +409,57 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = mbar_wait(final_bar, 0, a.status, kSiteDq);  // single phase: every MMA has completed
             ok = __all_sync(0xffffffffu, ok);
         }
+        // Epilogue: dQ (times the scale) is staged in the Q / dO tiles' shared memory, which no MMA reads any
+        // more (every S and dP product completed before the last dS was written), as 128-byte-swizzled
+        // panels of 128 rows -- 64 columns in bf16, 32 in fp32 -- and written by TMA bulk stores, which clip
+        // rows past N and columns past the caller's D.  (A thread storing its own row to global memory
+        // touches a different 128-byte line per lane and instruction, and took ~1.3 us per CTA.)
+        static_assert(DQ * 4 <= 4 * D, "staging fits in the Q and dO tiles");
         if (ok) {
             tc_fence_after();
-            constexpr int kCols = DQ / kComputeWG;  // this warpgroup's columns of dQ
-            constexpr int kChunk = kCols < 32 ? kCols : 32;
-            uint32_t v[kChunk];
+            constexpr int kCols = DQ / kComputeWG;  // this warpgroup's columns of dQ (64 or 96)
+            static_assert(kCols % 32 == 0, "32-column TMEM loads");
+            const int sw = r & 7;
+            uint32_t v[32];
 #pragma unroll
-            for (int ch = 0; ch < kCols / kChunk; ++ch) {
-                const int col = g * kCols + ch * kChunk;
-                tmem_ld_n<kChunk>(tmem + lane_base + kColDQ + col, v);
+            for (int ch = 0; ch < kCols / 32; ++ch) {
+                const int col = g * kCols + ch * 32;  // within this CTA's DQ columns
+                tmem_ld32(tmem + lane_base + kColDQ + col, v);
                 tmem_wait_ld();
 #pragma unroll
-                for (int t = 0; t < kChunk; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * a.scale);
-                if (valid) {
-                    if (a.grad_bf16) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.dq) +
-                                                               ((size_t)bh * N + row) * Dr + dq0 + col);
+                for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * a.scale);
+                if (a.grad_bf16) {
+                    // 32 columns = 4 chunks of a 64-column panel's row
+                    uint8_t *prow = smem + (col / 64) * (kBM * 128) + r * 128;
+                    const int c0 = (col % 64) / 8;
 #pragma unroll
-                        for (int v4 = 0; v4 < kChunk / 8; ++v4) {
-                            if (dq0 + col + 8 * v4 >= Dr) break;
-                            uint4 w;
-                            w.x = pack_bf16x2(__uint_as_float(v[v4 * 8 + 0]), __uint_as_float(v[v4 * 8 + 1]));
-                            w.y = pack_bf16x2(__uint_as_float(v[v4 * 8 + 2]), __uint_as_float(v[v4 * 8 + 3]));
-                            w.z = pack_bf16x2(__uint_as_float(v[v4 * 8 + 4]), __uint_as_float(v[v4 * 8 + 5]));
-                            w.w = pack_bf16x2(__uint_as_float(v[v4 * 8 + 6]), __uint_as_float(v[v4 * 8 + 7]));
-                            dst[v4] = w;
-                        }
-                    } else {
-                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.dq) +
-                                                                 ((size_t)bh * N + row) * Dr + dq0 + col);
+                    for (int c = 0; c < 4; ++c)
+                        st_shared_v4(prow + (((c0 + c) ^ sw) << 4),
+                                     pack_bf16x2(__uint_as_float(v[8 * c + 0]), __uint_as_float(v[8 * c + 1])),
+                                     pack_bf16x2(__uint_as_float(v[8 * c + 2]), __uint_as_float(v[8 * c + 3])),
+                                     pack_bf16x2(__uint_as_float(v[8 * c + 4]), __uint_as_float(v[8 * c + 5])),
+                                     pack_bf16x2(__uint_as_float(v[8 * c + 6]), __uint_as_float(v[8 * c + 7])));
+                } else {
+                    // 32 columns = one 32-column fp32 panel's row
+                    uint8_t *prow = smem + (col / 32) * (kBM * 128) + r * 128;
 #pragma unroll
-                        for (int v4 = 0; v4 < kChunk / 4; ++v4)
-                            if (dq0 + col + 4 * v4 < Dr) dst[v4] = make_float4(__uint_as_float(v[v4 * 4 + 0]), __uint_as_float(v[v4 * 4 + 1]),
-                                                  __uint_as_float(v[v4 * 4 + 2]), __uint_as_float(v[v4 * 4 + 3]));
-                    }
+                    for (int c = 0; c < 8; ++c)
+                        st_shared_v4(prow + ((c ^ sw) << 4), v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
                 }
             }
+        } else if (lane == 0) {
+            epi_abort = 1;
+        }
+        fence_proxy_async_smem();  // the staged tile is read by the TMA (async proxy)
+        asm volatile("bar.sync 1, %0;" ::"r"(128 * kComputeWG) : "memory");
+        if (threadIdx.x == 32 * kFirstComputeWarp && !epi_abort) {
+            const int n_panels = a.grad_bf16 ? DQ / 64 : DQ / 32;
+            const int pw = a.grad_bf16 ? 64 : 32;  // panel width in elements
+            for (int p = 0; p < n_panels; ++p)
+                if (dq0 + p * pw < Dr)  // a panel wholly past the caller's D is not stored
+                    tma_store_3d(&tmap_dq, smem + p * (kBM * 128), dq0 + p * pw, q_tile * kBM, bh);
+            tma_store_commit();
+            tma_store_wait_read();  // the CTA's shared memory must outlive the stores' reads
         }
     }
 
@@ -455,25 +473,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, int DQ, bool QT, int NSLOT>
 cudaError_t launch_spec(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                        const CUtensorMap &tdo, const CUtensorMap &to, cudaStream_t s) {
+                        const CUtensorMap &tdo, const CUtensorMap &to, const CUtensorMap &tdq, cudaStream_t s) {
     using L = DqSmem<D, NSLOT>;
     static_assert(L::kAlloc <= 232448, "shared memory budget");
     auto kern = bwd_dq_kernel<D, DQ, QT, NSLOT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     dim3 grid(((a.N + kBM - 1) / kBM) * a.H * a.B, D / DQ);
-    kern<<<grid, kThreads, L::kAlloc, s>>>(tq, tk, tv, tdo, to, a);
+    kern<<<grid, kThreads, L::kAlloc, s>>>(tq, tk, tv, tdo, to, tdq, a);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_dq(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                          const CUtensorMap &tdo, const CUtensorMap &to, cudaStream_t s) {
+                          const CUtensorMap &tdo, const CUtensorMap &to, const CUtensorMap &tdq, cudaStream_t s) {
     switch (kernel_head_dim(a.D)) {
-        case 128: return launch_spec<128, 128, true, 8>(a, tq, tk, tv, tdo, to, s);
-        case 192: return launch_spec<192, 192, false, 5>(a, tq, tk, tv, tdo, to, s);
-        case 256: return launch_spec<256, 128, false, 3>(a, tq, tk, tv, tdo, to, s);
+        case 128: return launch_spec<128, 128, true, 8>(a, tq, tk, tv, tdo, to, tdq, s);
+        case 192: return launch_spec<192, 192, false, 5>(a, tq, tk, tv, tdo, to, tdq, s);
+        case 256: return launch_spec<256, 128, false, 3>(a, tq, tk, tv, tdo, to, tdq, s);
         default: return cudaErrorInvalidValue;
     }
 }

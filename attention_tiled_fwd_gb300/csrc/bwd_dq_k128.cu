@@ -69,7 +69,8 @@ struct K128Smem {
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_k128_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                        const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
-                       const __grid_constant__ CUtensorMap tmap_o, BwdArgs a) {
+                       const __grid_constant__ CUtensorMap tmap_o, const __grid_constant__ CUtensorMap tmap_dq,
+                       BwdArgs a) {
     using L = K128Smem;
     constexpr uint32_t kTmemCols = 512;
     // TMEM columns: S = [0, 128) and dP = [128, 256), each single-buffered and released as soon as every
@@ -102,6 +103,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *o_full = a_final + 1;          // O's tile landed
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kTmemHolderOff);
 
+    __shared__ int epi_abort;  // a compute warp's wait ran out: the epilogue stores nothing
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int rank, bh;
     tile_order((a.N + kBM - 1) / kBM, a.B * a.H, a.causal, &rank, &bh);
@@ -111,6 +113,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_kv = (kv_end + kBN - 1) / kBN;  // >= 1
 
     if (threadIdx.x == 0) {
+        epi_abort = 0;
         mbar_init(q_full, 1);
         for (int s = 0; s < kNSlot; ++s) {
             mbar_init(&slot_full[s], 1);
@@ -358,37 +361,48 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = mbar_wait(final_bar, 0, a.status, kSiteDq);  // single phase: every MMA has completed
             ok = __all_sync(0xffffffffu, ok);
         }
+        // Epilogue: dQ (times the softmax scale) staged in the Q / dO tiles' shared memory, which no MMA reads
+        // any more, as 128-byte-swizzled panels of 128 rows (one of 64 bf16 columns, or two of 32 fp32
+        // columns), then written by TMA bulk stores that clip rows past N and columns past the caller's D.
         if (ok) {
             tc_fence_after();
-            // this warpgroup's 16 columns of dQ, times the softmax scale
+            // this warpgroup's 16 columns of dQ
             uint32_t v[16];
             tmem_ld16(tmem + lane_base + kColDQ + 16 * g, v);
             tmem_wait_ld();
-            if (valid) {
 #pragma unroll
-                for (int t = 0; t < 16; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * a.scale);
-                if (a.grad_bf16) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.dq) +
-                                                           ((size_t)bh * N + row) * Dr + 16 * g);
+            for (int t = 0; t < 16; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * a.scale);
+            const int sw = r & 7;
+            if (a.grad_bf16) {
+                uint8_t *prow = smem + r * 128;  // chunks 2g, 2g + 1 of the 64-column panel
 #pragma unroll
-                    for (int v4 = 0; v4 < 2; ++v4) {
-                        if (16 * g + 8 * v4 >= Dr) break;
-                        uint4 o4;
-                        o4.x = pack_bf16x2(__uint_as_float(v[v4 * 8 + 0]), __uint_as_float(v[v4 * 8 + 1]));
-                        o4.y = pack_bf16x2(__uint_as_float(v[v4 * 8 + 2]), __uint_as_float(v[v4 * 8 + 3]));
-                        o4.z = pack_bf16x2(__uint_as_float(v[v4 * 8 + 4]), __uint_as_float(v[v4 * 8 + 5]));
-                        o4.w = pack_bf16x2(__uint_as_float(v[v4 * 8 + 6]), __uint_as_float(v[v4 * 8 + 7]));
-                        dst[v4] = o4;
-                    }
-                } else {
-                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.dq) +
-                                                             ((size_t)bh * N + row) * Dr + 16 * g);
+                for (int c = 0; c < 2; ++c)
+                    st_shared_v4(prow + (((2 * g + c) ^ sw) << 4),
+                                 pack_bf16x2(__uint_as_float(v[8 * c + 0]), __uint_as_float(v[8 * c + 1])),
+                                 pack_bf16x2(__uint_as_float(v[8 * c + 2]), __uint_as_float(v[8 * c + 3])),
+                                 pack_bf16x2(__uint_as_float(v[8 * c + 4]), __uint_as_float(v[8 * c + 5])),
+                                 pack_bf16x2(__uint_as_float(v[8 * c + 6]), __uint_as_float(v[8 * c + 7])));
+            } else {
+                uint8_t *prow = smem + (g >> 1) * (kBM * 128) + r * 128;  // chunks 4 (g % 2) .. + 3 of panel g / 2
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4)
-                        if (16 * g + 4 * v4 < Dr) dst[v4] = make_float4(__uint_as_float(v[v4 * 4 + 0]), __uint_as_float(v[v4 * 4 + 1]),
-                                              __uint_as_float(v[v4 * 4 + 2]), __uint_as_float(v[v4 * 4 + 3]));
-                }
+                for (int c = 0; c < 4; ++c)
+                    st_shared_v4(prow + (((4 * (g & 1) + c) ^ sw) << 4), v[4 * c], v[4 * c + 1], v[4 * c + 2],
+                                 v[4 * c + 3]);
             }
+        } else if (lane == 0) {
+            epi_abort = 1;
+        }
+        fence_proxy_async_smem();  // the staged tile is read by the TMA (async proxy)
+        asm volatile("bar.sync 1, %0;" ::"r"(128 * kComputeWG) : "memory");
+        if (threadIdx.x == 32 * kFirstComputeWarp && !epi_abort) {
+            if (a.grad_bf16) {
+                tma_store_3d(&tmap_dq, smem, 0, q_tile * kBM, bh);
+            } else {
+                tma_store_3d(&tmap_dq, smem, 0, q_tile * kBM, bh);
+                if (Dr > 32) tma_store_3d(&tmap_dq, smem + kBM * 128, 32, q_tile * kBM, bh);
+            }
+            tma_store_commit();
+            tma_store_wait_read();  // the CTA's shared memory must outlive the stores' reads
         }
     }
 
@@ -403,7 +417,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_bwd_dq_k128(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                               const CUtensorMap &tdo, const CUtensorMap &to, cudaStream_t s) {
+                               const CUtensorMap &tdo, const CUtensorMap &to, const CUtensorMap &tdq,
+                               cudaStream_t s) {
     using L = K128Smem;
     static_assert(L::kAlloc <= 232448, "shared memory budget");
     if (kernel_head_dim(a.D) != kD) return cudaErrorInvalidValue;
@@ -411,7 +426,7 @@ cudaError_t launch_bwd_dq_k128(const BwdArgs &a, const CUtensorMap &tq, const CU
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     dim3 grid(((a.N + kBM - 1) / kBM) * a.H * a.B);
-    kern<<<grid, kThreads, L::kAlloc, s>>>(tq, tk, tv, tdo, to, a);
+    kern<<<grid, kThreads, L::kAlloc, s>>>(tq, tk, tv, tdo, to, tdq, a);
     return cudaGetLastError();
 }
 

@@ -107,6 +107,21 @@ int check_shape(int B, int H, int N, int D, float scale) {
     return FA_OK;
 }
 
+// [B*H, N, D] bf16 or fp32 tensor, box {128 bytes of a row, rows, 1}, 128-byte swizzle, zero fill out of
+// bounds (loads) and clipping (stores).
+int encode_3d(CUtensorMap *map, const void *base, int BH, int N, int D, int box_rows, bool f32) {
+    const int elt = f32 ? 4 : 2;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)D * elt, (cuuint64_t)N * D * elt};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / elt), (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                          const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
 // [B*H, N, D] bf16 tensor, box {64, rows, 1}, 128-byte swizzle, zero fill out of bounds.
 int encode_bf16_3d(CUtensorMap *map, const void *base, int BH, int N, int D, int box_rows) {
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
@@ -193,17 +208,19 @@ extern "C" int fa_backward_dq(const void *q, const void *k, const void *v, const
     if (rc != FA_OK) return rc;
     BwdArgs a{q, k, v, o, dO, lse, delta, dq, nullptr, nullptr, B, H, N, D, scale, scale * log2e(),
               causal ? 1 : 0, grad_dtype == FA_BF16 ? 1 : 0, st->status_word};
-    CUtensorMap tq, tk, tv, tdo, to;
+    CUtensorMap tq, tk, tv, tdo, to, tdq;
     // D <= 64 runs the 128-key-tile kernel (its score products are N = 128 MMAs); wider heads the 64-key one
     const int Dk = kernel_head_dim(D);
     const int kv_rows = Dk == 64 ? 128 : kDqKRows;
     if (encode_bf16_3d(&tq, q, B * H, N, D, 128) != FA_OK ||
         encode_bf16_3d(&tk, k, B * H, N, D, kv_rows) != FA_OK ||
         encode_bf16_3d(&tv, v, B * H, N, D, kv_rows) != FA_OK ||
-        encode_bf16_3d(&tdo, dO, B * H, N, D, 128) != FA_OK || encode_bf16_3d(&to, o, B * H, N, D, 128) != FA_OK)
+        encode_bf16_3d(&tdo, dO, B * H, N, D, 128) != FA_OK || encode_bf16_3d(&to, o, B * H, N, D, 128) != FA_OK ||
+        encode_3d(&tdq, dq, B * H, N, D, 128, grad_dtype == FA_F32) != FA_OK)
         return FA_ERR_CUDA;
-    cudaError_t e = Dk == 64 ? launch_bwd_dq_k128(a, tq, tk, tv, tdo, to, reinterpret_cast<cudaStream_t>(stream))
-                             : launch_bwd_dq(a, tq, tk, tv, tdo, to, reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e = Dk == 64
+                        ? launch_bwd_dq_k128(a, tq, tk, tv, tdo, to, tdq, reinterpret_cast<cudaStream_t>(stream))
+                        : launch_bwd_dq(a, tq, tk, tv, tdo, to, tdq, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

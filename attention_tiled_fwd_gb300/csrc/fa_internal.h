@@ -127,13 +127,15 @@ cudaError_t launch_fwd_bf16(const FwdArgs &a, const CUtensorMap &tq, const CUten
                             const CUtensorMap &tv, cudaStream_t s);
 cudaError_t launch_fwd_bf16_pair(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
                                  const CUtensorMap &tv, cudaStream_t s);
-// the dQ kernels also take O's tensor map (128-row boxes): its tile is staged for D_i = rowsum(dO * O)
+// The dQ kernels also take O's tensor map (128-row boxes; its tile is staged for D_i = rowsum(dO * O))
+// and dQ's (grad dtype, 128-byte boxes of 128 rows, 128-byte swizzle: the TMA stores of the epilogue).
 cudaError_t launch_bwd_dq(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
-                          const CUtensorMap &tv, const CUtensorMap &tdo, const CUtensorMap &to, cudaStream_t s);
+                          const CUtensorMap &tv, const CUtensorMap &tdo, const CUtensorMap &to,
+                          const CUtensorMap &tdq, cudaStream_t s);
 // bwd_dq_k128.cu: the dQ kernel for D = 64 with 128-row K / V tiles (TMA boxes of 128 rows)
 cudaError_t launch_bwd_dq_k128(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
                                const CUtensorMap &tv, const CUtensorMap &tdo, const CUtensorMap &to,
-                               cudaStream_t s);
+                               const CUtensorMap &tdq, cudaStream_t s);
 // bwd_dkdv_q128.cu: the dK/dV kernel for D = 64 with 128-row Q / dO tiles (TMA boxes of 128 rows)
 cudaError_t launch_bwd_dkdv_q128(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
                                  const CUtensorMap &tv, const CUtensorMap &tdo, cudaStream_t s);
