@@ -90,6 +90,7 @@ template <int D, int DO, int NB, int NSLOT, int kStatSlots>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
+                    const __grid_constant__ CUtensorMap tmap_dk, const __grid_constant__ CUtensorMap tmap_dv,
                     BwdArgs a) {
     using L = DkdvSmem<D, NSLOT, kStatSlots>;
     constexpr int kPanels = D / 64;
@@ -130,6 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *a_final = final_bar + 1;   // issuer A: every S^T / dP^T MMA has completed
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kTmemHolderOff);
 
+    __shared__ int epi_abort;  // a compute warp's wait ran out: the epilogue stores nothing
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int rank, bh;
     tile_order((a.N + kBN - 1) / kBN, a.B * a.H, a.causal, &rank, &bh);
@@ -142,6 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int Dr = a.D;                   // row stride and real columns (<= D; the rest are zeros)
 
     if (threadIdx.x == 0) {
+        epi_abort = 0;
         mbar_init(kv_full, 1);
         for (int s = 0; s < NSLOT; ++s) {
             mbar_init(&slot_full[s], 1);
@@ -424,47 +427,62 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = mbar_wait(final_bar, 0, a.status, kSiteDone);
             ok = __all_sync(0xffffffffu, ok);
         }
+        // Epilogue: dV and dK (dK times the scale its dS^T operands left out) are staged in the K / V tiles'
+        // and the ring's shared memory, which nothing reads any more once every MMA has completed, as
+        // 128-byte-swizzled panels of 128 rows (64 bf16 or 32 fp32 columns; dV's panels first), and written
+        // by TMA bulk stores that clip rows past N and columns past the caller's D.
+        const int n_panels = a.grad_bf16 ? DO / 64 : DO / 32;  // per output
+        static_assert(2 * DO * 4 * kBN <= 2 * L::kKVBytes + NSLOT * L::kTileBytes, "staging fits");
         if (ok) {
             tc_fence_after();
-            const bool valid = key < N;
             // the first half of the warpgroups writes dV, the second dK; each its share of the D columns
             constexpr int kCols = DO / (kComputeWG / 2);
+            static_assert(kCols % 32 == 0, "32-column TMEM loads");
             const bool is_dv = g < kComputeWG / 2;
             const int c0 = (g % (kComputeWG / 2)) * kCols;
             const uint32_t col = (is_dv ? kColDV : kColDK) + c0;
-            void *outp = is_dv ? a.dv : a.dk;
             const float osc = is_dv ? 1.f : sc;  // dK picks up the scale its dS^T operands left out
+            uint8_t *stage = smem + (is_dv ? 0 : n_panels) * (kBN * 128) + r * 128;
+            const int sw = r & 7;
             uint32_t v[32];
 #pragma unroll
             for (int ch = 0; ch < kCols / 32; ++ch) {
                 tmem_ld32(tmem + lane_base + col + ch * 32, v);
                 tmem_wait_ld();
-                if (!valid) continue;
 #pragma unroll
                 for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * osc);
-                const int gc = do0 + c0 + ch * 32;  // first global column of this chunk
+                const int oc = c0 + ch * 32;  // column within this CTA's DO columns
                 if (a.grad_bf16) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(outp) +
-                                                           ((size_t)bh * N + key) * Dr + gc);
+                    uint8_t *prow = stage + (oc / 64) * (kBN * 128);
+                    const int cb = (oc % 64) / 8;
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4) {
-                        if (gc + 8 * v4 >= Dr) break;
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(v[v4 * 8 + 0]), __uint_as_float(v[v4 * 8 + 1]));
-                        w.y = pack_bf16x2(__uint_as_float(v[v4 * 8 + 2]), __uint_as_float(v[v4 * 8 + 3]));
-                        w.z = pack_bf16x2(__uint_as_float(v[v4 * 8 + 4]), __uint_as_float(v[v4 * 8 + 5]));
-                        w.w = pack_bf16x2(__uint_as_float(v[v4 * 8 + 6]), __uint_as_float(v[v4 * 8 + 7]));
-                        dst[v4] = w;
-                    }
+                    for (int c = 0; c < 4; ++c)
+                        st_shared_v4(prow + (((cb + c) ^ sw) << 4),
+                                     pack_bf16x2(__uint_as_float(v[8 * c + 0]), __uint_as_float(v[8 * c + 1])),
+                                     pack_bf16x2(__uint_as_float(v[8 * c + 2]), __uint_as_float(v[8 * c + 3])),
+                                     pack_bf16x2(__uint_as_float(v[8 * c + 4]), __uint_as_float(v[8 * c + 5])),
+                                     pack_bf16x2(__uint_as_float(v[8 * c + 6]), __uint_as_float(v[8 * c + 7])));
                 } else {
-                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(outp) +
-                                                             ((size_t)bh * N + key) * Dr + gc);
+                    uint8_t *prow = stage + (oc / 32) * (kBN * 128);
 #pragma unroll
-                    for (int v4 = 0; v4 < 8; ++v4)
-                        if (gc + 4 * v4 < Dr) dst[v4] = make_float4(__uint_as_float(v[v4 * 4 + 0]), __uint_as_float(v[v4 * 4 + 1]),
-                                              __uint_as_float(v[v4 * 4 + 2]), __uint_as_float(v[v4 * 4 + 3]));
+                    for (int c = 0; c < 8; ++c)
+                        st_shared_v4(prow + ((c ^ sw) << 4), v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
                 }
             }
+        } else if (lane == 0) {
+            epi_abort = 1;
+        }
+        fence_proxy_async_smem();  // the staged tiles are read by the TMA (async proxy)
+        asm volatile("bar.sync 1, %0;" ::"r"(128 * kComputeWG) : "memory");
+        if (threadIdx.x == 32 * kFirstComputeWarp && !epi_abort) {
+            const int pw = a.grad_bf16 ? 64 : 32;  // panel width in elements
+            for (int p = 0; p < n_panels; ++p) {
+                if (do0 + p * pw >= Dr) break;  // panels wholly past the caller's D are not stored
+                tma_store_3d(&tmap_dv, smem + p * (kBN * 128), do0 + p * pw, k_tile * kBN, bh);
+                tma_store_3d(&tmap_dk, smem + (n_panels + p) * (kBN * 128), do0 + p * pw, k_tile * kBN, bh);
+            }
+            tma_store_commit();
+            tma_store_wait_read();  // the CTA's shared memory must outlive the stores' reads
         }
     }
 
@@ -478,25 +496,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, int DO, int NB, int NSLOT, int STATS>
 cudaError_t launch_spec(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                        const CUtensorMap &tdo, cudaStream_t s) {
+                        const CUtensorMap &tdo, const CUtensorMap &tdk, const CUtensorMap &tdv, cudaStream_t s) {
     using L = DkdvSmem<D, NSLOT, STATS>;
     static_assert(L::kAlloc <= 232448, "shared memory budget");
     auto kern = bwd_dkdv_kernel<D, DO, NB, NSLOT, STATS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     dim3 grid(((a.N + kBN - 1) / kBN) * a.H * a.B, D / DO);
-    kern<<<grid, kThreads, L::kAlloc, s>>>(tq, tk, tv, tdo, a);
+    kern<<<grid, kThreads, L::kAlloc, s>>>(tq, tk, tv, tdo, tdk, tdv, a);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_dkdv(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                            const CUtensorMap &tdo, cudaStream_t s) {
+                            const CUtensorMap &tdo, const CUtensorMap &tdk, const CUtensorMap &tdv, cudaStream_t s) {
     switch (kernel_head_dim(a.D)) {
-        case 128: return launch_spec<128, 128, 2, 8, 4>(a, tq, tk, tv, tdo, s);
-        case 192: return launch_spec<192, 192, 1, 5, 4>(a, tq, tk, tv, tdo, s);
-        case 256: return launch_spec<256, 128, 2, 3, 3>(a, tq, tk, tv, tdo, s);
+        case 128: return launch_spec<128, 128, 2, 8, 4>(a, tq, tk, tv, tdo, tdk, tdv, s);
+        case 192: return launch_spec<192, 192, 1, 5, 4>(a, tq, tk, tv, tdo, tdk, tdv, s);
+        case 256: return launch_spec<256, 128, 2, 3, 3>(a, tq, tk, tv, tdo, tdk, tdv, s);
         default: return cudaErrorInvalidValue;
     }
 }

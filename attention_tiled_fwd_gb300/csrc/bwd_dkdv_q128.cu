@@ -64,6 +64,7 @@ struct Q128Smem {
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_q128_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                          const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
+                         const __grid_constant__ CUtensorMap tmap_dk, const __grid_constant__ CUtensorMap tmap_dv,
                          BwdArgs a) {
     using L = Q128Smem;
     constexpr uint32_t kTmemCols = 512;
@@ -95,6 +96,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *a_final = final_bar + 1;              // issuer A: every S^T / dP^T MMA has completed
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kTmemHolderOff);
 
+    __shared__ int epi_abort;  // a compute warp's wait ran out: the epilogue stores nothing
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int rank, bh;
     tile_order((a.N + kBN - 1) / kBN, a.B * a.H, a.causal, &rank, &bh);
@@ -105,6 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_q = n_q_total - q_begin;       // >= 1
 
     if (threadIdx.x == 0) {
+        epi_abort = 0;
         mbar_init(kv_full, 1);
         for (int s = 0; s < kNSlot; ++s) {
             mbar_init(&slot_full[s], 1);
@@ -373,44 +376,53 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = mbar_wait(final_bar, 0, a.status, kSiteDone);
             ok = __all_sync(0xffffffffu, ok);
         }
+        // Epilogue: dV and dK (dK times the scale its dS^T operands left out) are staged in the K / V tiles'
+        // and the ring's shared memory, which nothing reads any more once every MMA has completed, as
+        // 128-byte-swizzled panels of 128 rows (one of 64 bf16 or two of 32 fp32 columns per output; dV's
+        // first), and written by TMA bulk stores that clip rows past N and columns past the caller's D.
+        const int n_panels = a.grad_bf16 ? 1 : 2;  // per output
+        const int Dr = a.D;
         if (ok) {
             tc_fence_after();
-            const bool valid = key < N;
             // warpgroups 0, 1 write dV (32 columns each), warpgroups 2, 3 write dK
             const bool is_dv = g < 2;
             const int c0 = (g & 1) * 32;
-            void *outp = is_dv ? a.dv : a.dk;
             const float osc = is_dv ? 1.f : sc;  // dK picks up the scale its dS^T operands left out
             uint32_t v[32];
             tmem_ld32(tmem + lane_base + (is_dv ? kColDV : kColDK) + c0, v);
             tmem_wait_ld();
-            // row stride and real columns: the caller's D (a multiple of 8, at most 64)
-            const int Dr = a.D;
-            if (valid) {
 #pragma unroll
-                for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * osc);
-                if (a.grad_bf16) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(outp) +
-                                                           ((size_t)bh * N + key) * Dr + c0);
+            for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * osc);
+            uint8_t *stage = smem + (is_dv ? 0 : n_panels) * (kBN * 128) + r * 128;
+            const int sw = r & 7;
+            if (a.grad_bf16) {
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4) {
-                        if (c0 + 8 * v4 >= Dr) break;
-                        uint4 o4;
-                        o4.x = pack_bf16x2(__uint_as_float(v[v4 * 8 + 0]), __uint_as_float(v[v4 * 8 + 1]));
-                        o4.y = pack_bf16x2(__uint_as_float(v[v4 * 8 + 2]), __uint_as_float(v[v4 * 8 + 3]));
-                        o4.z = pack_bf16x2(__uint_as_float(v[v4 * 8 + 4]), __uint_as_float(v[v4 * 8 + 5]));
-                        o4.w = pack_bf16x2(__uint_as_float(v[v4 * 8 + 6]), __uint_as_float(v[v4 * 8 + 7]));
-                        dst[v4] = o4;
-                    }
-                } else {
-                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(outp) +
-                                                             ((size_t)bh * N + key) * Dr + c0);
+                for (int c = 0; c < 4; ++c)
+                    st_shared_v4(stage + (((4 * (g & 1) + c) ^ sw) << 4),
+                                 pack_bf16x2(__uint_as_float(v[8 * c + 0]), __uint_as_float(v[8 * c + 1])),
+                                 pack_bf16x2(__uint_as_float(v[8 * c + 2]), __uint_as_float(v[8 * c + 3])),
+                                 pack_bf16x2(__uint_as_float(v[8 * c + 4]), __uint_as_float(v[8 * c + 5])),
+                                 pack_bf16x2(__uint_as_float(v[8 * c + 6]), __uint_as_float(v[8 * c + 7])));
+            } else {
+                uint8_t *prow = stage + (g & 1) * (kBN * 128);
 #pragma unroll
-                    for (int v4 = 0; v4 < 8; ++v4)
-                        if (c0 + 4 * v4 < Dr) dst[v4] = make_float4(__uint_as_float(v[v4 * 4 + 0]), __uint_as_float(v[v4 * 4 + 1]),
-                                              __uint_as_float(v[v4 * 4 + 2]), __uint_as_float(v[v4 * 4 + 3]));
-                }
+                for (int c = 0; c < 8; ++c)
+                    st_shared_v4(prow + ((c ^ sw) << 4), v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
             }
+        } else if (lane == 0) {
+            epi_abort = 1;
+        }
+        fence_proxy_async_smem();  // the staged tiles are read by the TMA (async proxy)
+        asm volatile("bar.sync 1, %0;" ::"r"(128 * kComputeWG) : "memory");
+        if (threadIdx.x == 32 * kFirstComputeWarp && !epi_abort) {
+            const int pw = a.grad_bf16 ? 64 : 32;  // panel width in elements
+            for (int p = 0; p < n_panels; ++p) {
+                if (p * pw >= Dr) break;  // a panel wholly past the caller's D is not stored
+                tma_store_3d(&tmap_dv, smem + p * (kBN * 128), p * pw, k_tile * kBN, bh);
+                tma_store_3d(&tmap_dk, smem + (n_panels + p) * (kBN * 128), p * pw, k_tile * kBN, bh);
+            }
+            tma_store_commit();
+            tma_store_wait_read();  // the CTA's shared memory must outlive the stores' reads
         }
     }
 
@@ -425,7 +437,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_bwd_dkdv_q128(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
-                                 const CUtensorMap &tv, const CUtensorMap &tdo, cudaStream_t s) {
+                                 const CUtensorMap &tv, const CUtensorMap &tdo, const CUtensorMap &tdk,
+                                 const CUtensorMap &tdv, cudaStream_t s) {
     using L = Q128Smem;
     static_assert(L::kAlloc <= 232448, "shared memory budget");
     if (kernel_head_dim(a.D) != kD) return cudaErrorInvalidValue;
@@ -433,7 +446,7 @@ cudaError_t launch_bwd_dkdv_q128(const BwdArgs &a, const CUtensorMap &tq, const 
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     dim3 grid(((a.N + kBN - 1) / kBN) * a.H * a.B);
-    kern<<<grid, kThreads, L::kAlloc, s>>>(tq, tk, tv, tdo, a);
+    kern<<<grid, kThreads, L::kAlloc, s>>>(tq, tk, tv, tdo, tdk, tdv, a);
     return cudaGetLastError();
 }
 

@@ -241,16 +241,19 @@ extern "C" int fa_backward_dkdv(const void *q, const void *k, const void *v, con
     if (rc != FA_OK) return rc;
     BwdArgs a{q, k, v, nullptr, dO, lse, const_cast<float *>(delta), nullptr, dk, dv, B, H, N, D, scale,
               scale * log2e(), causal ? 1 : 0, grad_dtype == FA_BF16 ? 1 : 0, st->status_word};
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tdk, tdv;
     // D <= 64 runs the 128-query-tile kernel (its score products are N = 128 MMAs); wider heads the 64-query one
     const int Dk = kernel_head_dim(D);
     const int q_rows = Dk == 64 ? 128 : kDkdvQRows;
     if (encode_bf16_3d(&tq, q, B * H, N, D, q_rows) != FA_OK ||
         encode_bf16_3d(&tk, k, B * H, N, D, 128) != FA_OK || encode_bf16_3d(&tv, v, B * H, N, D, 128) != FA_OK ||
-        encode_bf16_3d(&tdo, dO, B * H, N, D, q_rows) != FA_OK)
+        encode_bf16_3d(&tdo, dO, B * H, N, D, q_rows) != FA_OK ||
+        encode_3d(&tdk, dk, B * H, N, D, 128, grad_dtype == FA_F32) != FA_OK ||
+        encode_3d(&tdv, dv, B * H, N, D, 128, grad_dtype == FA_F32) != FA_OK)
         return FA_ERR_CUDA;
-    cudaError_t e = Dk == 64 ? launch_bwd_dkdv_q128(a, tq, tk, tv, tdo, reinterpret_cast<cudaStream_t>(stream))
-                             : launch_bwd_dkdv(a, tq, tk, tv, tdo, reinterpret_cast<cudaStream_t>(stream));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = Dk == 64 ? launch_bwd_dkdv_q128(a, tq, tk, tv, tdo, tdk, tdv, s)
+                             : launch_bwd_dkdv(a, tq, tk, tv, tdo, tdk, tdv, s);
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

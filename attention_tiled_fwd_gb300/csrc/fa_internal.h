@@ -136,11 +136,15 @@ cudaError_t launch_bwd_dq(const BwdArgs &a, const CUtensorMap &tq, const CUtenso
 cudaError_t launch_bwd_dq_k128(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
                                const CUtensorMap &tv, const CUtensorMap &tdo, const CUtensorMap &to,
                                const CUtensorMap &tdq, cudaStream_t s);
+// The dK/dV kernels also take dK's and dV's tensor maps (grad dtype, 128-byte boxes of 128 rows, 128-byte
+// swizzle: the TMA stores of the epilogue).
 // bwd_dkdv_q128.cu: the dK/dV kernel for D = 64 with 128-row Q / dO tiles (TMA boxes of 128 rows)
 cudaError_t launch_bwd_dkdv_q128(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
-                                 const CUtensorMap &tv, const CUtensorMap &tdo, cudaStream_t s);
+                                 const CUtensorMap &tv, const CUtensorMap &tdo, const CUtensorMap &tdk,
+                                 const CUtensorMap &tdv, cudaStream_t s);
 cudaError_t launch_bwd_dkdv(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
-                            const CUtensorMap &tv, const CUtensorMap &tdo, cudaStream_t s);
+                            const CUtensorMap &tv, const CUtensorMap &tdo, const CUtensorMap &tdk,
+                            const CUtensorMap &tdv, cudaStream_t s);
 cudaError_t launch_selftest_timeout(int *status, int limit_us, cudaStream_t s);
 
 // Head dimension a bf16 kernel is built for: the smallest of 64, 128, 192, 256 that holds D.  Any
