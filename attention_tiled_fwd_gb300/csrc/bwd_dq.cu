@@ -74,8 +74,8 @@ struct DqSmem {
     static constexpr int kSlotOff = 2 * kQBytes;
     static constexpr int kOOff = kSlotOff + NSLOT * kTileBytes;
     // q_full, slot_full[NSLOT], slot_empty[NSLOT], s_full[2], ds_full[2], final, a_final, dq_done[2], qt_ready,
-    // o_full
-    static constexpr int kNumBars = 1 + 2 * NSLOT + 10;
+    // o_full, dp_full[2]
+    static constexpr int kNumBars = 1 + 2 * NSLOT + 12;
     static constexpr int kRest = kComputeWG * kBM * 4 + kNumBars * 8 + 16 + 1024;
     // O's tile is staged by TMA where it fits (D = 128): D_i is then summed from shared memory.  At larger D
     // the compute warps read the O and dO rows from global memory instead.
@@ -101,6 +101,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t kColDQ = 256, kColDS = 256 + DQ, kColQ = kColDS + 64;
     static_assert(kColQ + (QT ? D / 2 : 0) <= 512, "TMEM budget");
     static_assert(DQ % 64 == 0 && D % DQ == 0, "dQ columns per CTA: whole panels");
+    constexpr bool kSplitDp = !QT;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -113,13 +114,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *q_full = bars;
     uint64_t *slot_full = bars + 1;
     uint64_t *slot_empty = slot_full + NSLOT;
-    uint64_t *s_full = slot_empty + NSLOT;  // [2]: S_j and dP_j complete
+    uint64_t *s_full = slot_empty + NSLOT;  // [2]: S_j (and dP_j unless kSplitDp) complete
     uint64_t *ds_full = s_full + 2;         // [2]: dS_j written (and S_j, dP_j read)
     uint64_t *final_bar = ds_full + 2;  // issuer B: every dQ MMA has completed
     uint64_t *a_final = final_bar + 1;  // issuer A: every S / dP MMA has completed
     uint64_t *dq_done = a_final + 1;    // [2]: dQ_j completed (its dS buffer j % 2 is free)
     uint64_t *qt_ready = dq_done + 2;   // Q is in TMEM
     uint64_t *o_full = qt_ready + 1;    // O's tile landed (kOTile)
+    // [2]: dP_j complete, with its own barrier at D = 192, 256 (kSplitDp): P_j's exponentials then run while
+    // the dP product still executes, which measured 7-18 % faster there.  At D = 128 (Q in TMEM) s_full
+    // covers S_j and dP_j both: the split measured 10 % slower.
+    uint64_t *dp_full = o_full + 1;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kTmemHolderOff);
 
     __shared__ int epi_abort;  // a compute warp's wait ran out: the epilogue stores nothing
@@ -142,6 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&s_full[b], 1);
+            mbar_init(&dp_full[b], 1);
             mbar_init(&ds_full[b], 4 * kComputeWG);  // one arrive per compute warp
         }
         mbar_init(final_bar, 1);
@@ -218,29 +224,50 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t b = j & 1;
             // S[b], dP[b] last held tile j-2, which the compute warps have finished with
             if (j >= 2 && !(ok = warp_wait(&ds_full[b], ((j - 2) >> 1) & 1, a.status, kSiteDsFull))) break;
-            if (!(ok = warp_wait(&slot_full[k_slot], k_round & 1, a.status, kSiteSlotFull))) break;
-            if (!(ok = warp_wait(&slot_full[v_slot], v_round & 1, a.status, kSiteSlotFull))) break;
-            tc_fence_after();
-            const uint64_t k_desc = sdesc_sw128(slot_addr + k_slot * L::kTileBytes, 16, 1024);
-            const uint64_t v_desc = sdesc_sw128(slot_addr + v_slot * L::kTileBytes, 16, 1024);
-            if (leader) {
+            if constexpr (!kSplitDp) {
+                if (!(ok = warp_wait(&slot_full[k_slot], k_round & 1, a.status, kSiteSlotFull))) break;
+                if (!(ok = warp_wait(&slot_full[v_slot], v_round & 1, a.status, kSiteSlotFull))) break;
+                tc_fence_after();
+                const uint64_t k_desc = sdesc_sw128(slot_addr + k_slot * L::kTileBytes, 16, 1024);
+                const uint64_t v_desc = sdesc_sw128(slot_addr + v_slot * L::kTileBytes, 16, 1024);
+                if (leader) {
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    if constexpr (QT)
+                    for (int ks = 0; ks < D / 16; ++ks)
                         mma_ts(tmem + 64 * b, tmem + kColQ + ks * 8,
                                sdesc_add(k_desc, (ks >> 2) * (kBN * 128) + (ks & 3) * 32), idesc_sq, ks > 0);
-                    else
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        mma_ss(tmem + 128 + 64 * b, sdesc_add(do_desc, (ks >> 2) * (kBM * 128) + (ks & 3) * 32),
+                               sdesc_add(v_desc, (ks >> 2) * (kBN * 128) + (ks & 3) * 32), idesc_sq, ks > 0);
+                    mma_commit(&s_full[b]);
+                    mma_commit(&slot_empty[v_slot]);  // V_j is no longer needed
+                }
+                __syncwarp();
+            } else {
+                if (!(ok = warp_wait(&slot_full[k_slot], k_round & 1, a.status, kSiteSlotFull))) break;
+                tc_fence_after();
+                const uint64_t k_desc = sdesc_sw128(slot_addr + k_slot * L::kTileBytes, 16, 1024);
+                const uint64_t v_desc = sdesc_sw128(slot_addr + v_slot * L::kTileBytes, 16, 1024);
+                if (leader) {
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks)
                         mma_ss(tmem + 64 * b, sdesc_add(q_desc, (ks >> 2) * (kBM * 128) + (ks & 3) * 32),
                                sdesc_add(k_desc, (ks >> 2) * (kBN * 128) + (ks & 3) * 32), idesc_sq, ks > 0);
+                    mma_commit(&s_full[b]);
                 }
+                __syncwarp();
+                if (!(ok = warp_wait(&slot_full[v_slot], v_round & 1, a.status, kSiteSlotFull))) break;
+                tc_fence_after();
+                if (leader) {
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks)
-                    mma_ss(tmem + 128 + 64 * b, sdesc_add(do_desc, (ks >> 2) * (kBM * 128) + (ks & 3) * 32),
-                           sdesc_add(v_desc, (ks >> 2) * (kBN * 128) + (ks & 3) * 32), idesc_sq, ks > 0);
-                mma_commit(&s_full[b]);
-                mma_commit(&slot_empty[v_slot]);  // V_j is no longer needed
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        mma_ss(tmem + 128 + 64 * b, sdesc_add(do_desc, (ks >> 2) * (kBM * 128) + (ks & 3) * 32),
+                               sdesc_add(v_desc, (ks >> 2) * (kBN * 128) + (ks & 3) * 32), idesc_sq, ks > 0);
+                    mma_commit(&dp_full[b]);
+                    mma_commit(&slot_empty[v_slot]);  // V_j is no longer needed
+                }
+                __syncwarp();
             }
-            __syncwarp();
         }
         // Drain this warp's MMAs before TMEM can be released (immediate in the normal path).
         if (leader) mma_commit(a_final);
@@ -382,23 +409,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc_fence_after();
             }
-            uint32_t sraw[kHalf], praw[kHalf], dsk[kHalf / 2];
-            tmem_ld_n<kHalf>(tmem + lane_base + 64 * b + g * kHalf, sraw);
-            tmem_ld_n<kHalf>(tmem + lane_base + 128 + 64 * b + g * kHalf, praw);
-            tmem_wait_ld();
-            // dS / scale = P * (dP - D), on fp32 pairs (f32x2), two scores per instruction
+            uint32_t dsk[kHalf / 2];
+            if constexpr (!kSplitDp) {
+                uint32_t sraw[kHalf], praw[kHalf];
+                tmem_ld_n<kHalf>(tmem + lane_base + 64 * b + g * kHalf, sraw);
+                tmem_ld_n<kHalf>(tmem + lane_base + 128 + 64 * b + g * kHalf, praw);
+                tmem_wait_ld();
+                // dS / scale = P * (dP - D), on fp32 pairs (f32x2), two scores per instruction
 #pragma unroll
-            for (int i = 0; i < kHalf; i += 2) {
-                float p0, p1;
-                f2_unpack(f2_fma(f2_pack(__uint_as_float(sraw[i]), __uint_as_float(sraw[i + 1])), c2, nl2), p0, p1);
-                p0 = ex2_approx(p0);
-                p1 = ex2_approx(p1);
-                if (need_mask) {
-                    if (key0 + i > lim) p0 = 0.f;
-                    if (key0 + i + 1 > lim) p1 = 0.f;
+                for (int i = 0; i < kHalf; i += 2) {
+                    float p0, p1;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(sraw[i]), __uint_as_float(sraw[i + 1])), c2, nl2), p0, p1);
+                    p0 = ex2_approx(p0);
+                    p1 = ex2_approx(p1);
+                    if (need_mask) {
+                        if (key0 + i > lim) p0 = 0.f;
+                        if (key0 + i + 1 > lim) p1 = 0.f;
+                    }
+                    dsk[i / 2] = f2_to_bf16x2(
+                        f2_mul(f2_sub(f2_pack(__uint_as_float(praw[i]), __uint_as_float(praw[i + 1])), d2), f2_pack(p0, p1)));
                 }
-                dsk[i / 2] = f2_to_bf16x2(
-                    f2_mul(f2_sub(f2_pack(__uint_as_float(praw[i]), __uint_as_float(praw[i + 1])), d2), f2_pack(p0, p1)));
+            } else {
+                uint32_t sraw[kHalf], praw[kHalf];
+                uint64_t p2[kHalf / 2];
+                tmem_ld_n<kHalf>(tmem + lane_base + 64 * b + g * kHalf, sraw);
+                tmem_wait_ld();
+                // P = 2^(S c - L log2 e) while dP_j may still be executing, on fp32 pairs (f32x2)
+#pragma unroll
+                for (int i = 0; i < kHalf; i += 2) {
+                    float p0, p1;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(sraw[i]), __uint_as_float(sraw[i + 1])), c2, nl2), p0, p1);
+                    p0 = ex2_approx(p0);
+                    p1 = ex2_approx(p1);
+                    if (need_mask) {
+                        if (key0 + i > lim) p0 = 0.f;
+                        if (key0 + i + 1 > lim) p1 = 0.f;
+                    }
+                    p2[i / 2] = f2_pack(p0, p1);
+                }
+                ok = mbar_wait(&dp_full[b], (j >> 1) & 1, a.status, kSiteSFull);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tc_fence_after();
+                tmem_ld_n<kHalf>(tmem + lane_base + 128 + 64 * b + g * kHalf, praw);
+                tmem_wait_ld();
+                // dS / scale = P * (dP - D), two scores per instruction
+#pragma unroll
+                for (int i = 0; i < kHalf; i += 2)
+                    dsk[i / 2] = f2_to_bf16x2(
+                        f2_mul(f2_sub(f2_pack(__uint_as_float(praw[i]), __uint_as_float(praw[i + 1])), d2), p2[i / 2]));
             }
             tmem_st_n<kHalf / 2>(tmem + lane_base + kColDS + 32 * b + g * (kHalf / 2), dsk);
             tmem_wait_st();
