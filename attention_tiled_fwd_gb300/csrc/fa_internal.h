@@ -127,6 +127,9 @@ cudaError_t launch_fwd_bf16(const FwdArgs &a, const CUtensorMap &tq, const CUten
                             const CUtensorMap &tv, cudaStream_t s);
 cudaError_t launch_fwd_bf16_pair(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
                                  const CUtensorMap &tv, cudaStream_t s);
+// fwd_bf16_duo.cu: D = 64, the two-tile persistent forward with one issuer warp and one P buffer per tile
+cudaError_t launch_fwd_bf16_duo(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
+                                const CUtensorMap &tv, cudaStream_t s);
 // The dQ kernels also take O's tensor map (128-row boxes; its tile is staged for D_i = rowsum(dO * O))
 // and dQ's (grad dtype, 128-byte boxes of 128 rows, 128-byte swizzle: the TMA stores of the epilogue).
 cudaError_t launch_bwd_dq(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,

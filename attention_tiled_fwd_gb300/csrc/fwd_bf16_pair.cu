@@ -1,4 +1,5 @@
-// fwd_bf16_pair.cu -- bf16 attention forward, D in {64, 128}: each CTA owns a
+// fwd_bf16_pair.cu -- bf16 attention forward for D = 128 (D = 64 runs the
+// variant in fwd_bf16_duo.cu, with an issuer and a P buffer per tile): each CTA owns a
 // pair of 128-row query tiles of one (batch, head) and streams 128-key K/V
 // tiles past both.  Same algorithm as fwd_bf16.cu ("Learning Metal with
 // FlashAttention", section "FlashAttention"; metalworking "Flash Attention",
@@ -453,7 +454,6 @@ cudaError_t launch_spec(const FwdArgs &a, const CUtensorMap &tq, const CUtensorM
 cudaError_t launch_fwd_bf16_pair(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
                                  const CUtensorMap &tv, cudaStream_t s) {
     switch (kernel_head_dim(a.D)) {
-        case 64: return launch_spec<64, 10>(a, tq, tk, tv, s);
         case 128: return launch_spec<128, 5>(a, tq, tk, tv, s);
         default: return cudaErrorInvalidValue;
     }

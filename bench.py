@@ -113,7 +113,7 @@ def kernel_sources(kernel: str, D: int, dtype: str = "bf16"):
     if kernel == "fwd":
         if dtype == "f32":
             return [CSRC + "fwd_f32.cu", CSRC + "fa_internal.h"]
-        return [CSRC + "fwd_bf16.cu", CSRC + "fwd_bf16_pair.cu"] + common
+        return [CSRC + "fwd_bf16.cu", CSRC + ("fwd_bf16_duo.cu" if D == 64 else "fwd_bf16_pair.cu")] + common
     if kernel == "bwd_dq":
         return [CSRC + ("bwd_dq_k128.cu" if D == 64 else "bwd_dq.cu")] + common
     if kernel == "bwd_dkdv":
