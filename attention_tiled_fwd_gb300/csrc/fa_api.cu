@@ -181,12 +181,12 @@ extern "C" int fa_forward(const void *q, const void *k, const void *v, void *o, 
     if (dtype == FA_F32) {
         e = launch_fwd_f32(a, s);
     } else {
-        CUtensorMap tq, tk, tv;
+        CUtensorMap tq, tk, tv, to;
         const int bn = fwd_block_n(kernel_head_dim(D));
         if (encode_bf16_3d(&tq, q, B * H, N, D, 128) != FA_OK || encode_bf16_3d(&tk, k, B * H, N, D, bn) != FA_OK ||
-            encode_bf16_3d(&tv, v, B * H, N, D, bn) != FA_OK)
+            encode_bf16_3d(&tv, v, B * H, N, D, bn) != FA_OK || encode_bf16_3d(&to, o, B * H, N, D, 128) != FA_OK)
             return FA_ERR_CUDA;
-        e = launch_fwd_bf16(a, tq, tk, tv, s);
+        e = launch_fwd_bf16(a, tq, tk, tv, to, s);
     }
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

@@ -123,10 +123,12 @@ struct TmaPair {
 };
 
 cudaError_t launch_fwd_f32(const FwdArgs &a, cudaStream_t s);
+// `to`: O's tensor map (bf16, 64-column boxes of 128 rows, 128-byte swizzle), for the kernels whose
+// epilogue stores O by TMA
 cudaError_t launch_fwd_bf16(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
-                            const CUtensorMap &tv, cudaStream_t s);
+                            const CUtensorMap &tv, const CUtensorMap &to, cudaStream_t s);
 cudaError_t launch_fwd_bf16_pair(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
-                                 const CUtensorMap &tv, cudaStream_t s);
+                                 const CUtensorMap &tv, const CUtensorMap &to, cudaStream_t s);
 // fwd_bf16_duo.cu: D = 64, the two-tile persistent forward with one issuer warp and one P buffer per tile
 cudaError_t launch_fwd_bf16_duo(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
                                 const CUtensorMap &tv, cudaStream_t s);

@@ -402,14 +402,14 @@ cudaError_t launch_spec(const FwdArgs &a, const CUtensorMap &tq, const CUtensorM
 }  // namespace
 
 cudaError_t launch_fwd_bf16(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                            cudaStream_t s) {
+                            const CUtensorMap &to, cudaStream_t s) {
     switch (kernel_head_dim(a.D)) {
         // measured choice per head dimension: a persistent two-tile kernel wherever its TMEM
         // layout fits (D <= 128; at D = 128 non-causal it measured equal to this kernel at
         // N = 4096 and 5-13 % faster at N = 1024, 2048 and 16384); at D = 64 the variant with an
         // issuer and a P buffer per tile (7 % faster there, 12-15 % slower at D = 128 without P buffers)
         case 64: return launch_fwd_bf16_duo(a, tq, tk, tv, s);
-        case 128: return launch_fwd_bf16_pair(a, tq, tk, tv, s);
+        case 128: return launch_fwd_bf16_pair(a, tq, tk, tv, to, s);
         case 192: return launch_spec<192, 64, 7>(a, tq, tk, tv, s);
         case 256: return launch_spec<256, 64, 4>(a, tq, tk, tv, s);
         default: return cudaErrorInvalidValue;

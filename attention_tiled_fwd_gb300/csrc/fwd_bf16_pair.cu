@@ -46,7 +46,7 @@ constexpr int kFirstSoftmaxWarp = 2;
 constexpr int kThreads = 32 * kFirstSoftmaxWarp + 128 * kTiles;
 
 enum : int { kSiteQ = 61, kSiteSlotEmpty, kSiteSlotFull, kSiteSFull, kSitePFull, kSitePV, kSiteFinal, kSiteDrain,
-             kSiteQEmpty, kSiteOFree };
+             kSiteQEmpty, kSiteOFree, kSiteStage };
 
 template <int D, int NSLOT>
 struct PairSmem {
@@ -55,9 +55,11 @@ struct PairSmem {
     static constexpr int kSlotBytes = kBN * D * 2;  // one K or V tile
     static constexpr int kQOff = 0;
     static constexpr int kSlotOff = kTiles * kQBytes;
-    static constexpr int kBarOff = kSlotOff + NSLOT * kSlotBytes;
-    // q_full, q_empty, slot_full[NSLOT], slot_empty[NSLOT], per tile: s_full, p_full, pv_done, o_free; final
-    static constexpr int kNumBars = 2 + 2 * NSLOT + 4 * kTiles + 1;
+    static constexpr int kStageOff = kSlotOff + NSLOT * kSlotBytes;  // one query tile's O, staged for TMA stores
+    static constexpr int kBarOff = kStageOff + kQBytes;
+    // q_full, q_empty, slot_full[NSLOT], slot_empty[NSLOT], per tile: s_full, p_full, pv_done, o_free,
+    // stage_full; final, stage_free
+    static constexpr int kNumBars = 2 + 2 * NSLOT + 5 * kTiles + 2;
     static constexpr int kTmemHolderOff = kBarOff + kNumBars * 8;
     static constexpr int kAlloc = kTmemHolderOff + 16 + 1024;
 };
@@ -92,7 +94,8 @@ __device__ __forceinline__ PairBlock pair_block(const FwdArgs &a, int L, int n_b
 template <int D, int NSLOT>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-                         const __grid_constant__ CUtensorMap tmap_v, FwdArgs a) {
+                         const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_o,
+                         FwdArgs a) {
     using L = PairSmem<D, NSLOT>;
     constexpr int kPanels = L::kPanels;
     constexpr uint32_t kTmemCols = 512;
@@ -114,6 +117,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *pv_done = p_full + kTiles;    // [tile]: PV_X of step g complete
     uint64_t *o_free = pv_done + kTiles;    // [tile]: the epilogue has read O_X (phase = X's blocks with work)
     uint64_t *final_bar = o_free + kTiles;  // every MMA of the CTA has completed
+    // The epilogue of a query tile writes O into the one staging buffer and stores it by TMA.  Within a
+    // block tile A uses the buffer before tile B, so every role can count the uses from the blocks:
+    uint64_t *stage_full = final_bar + 1;      // [tile]: the tile's four warps have written the buffer
+    uint64_t *stage_free = stage_full + kTiles;  // the last store has finished reading it (phase = use)
+    uint8_t *stage = smem + L::kStageOff;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kTmemHolderOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -135,6 +143,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&o_free[x], 4);
         }
         mbar_init(final_bar, 1);
+        for (int x = 0; x < kTiles; ++x) mbar_init(&stage_full[x], 4);
+        mbar_init(stage_free, 1);
         fence_mbarrier_init();
     }
     if (warp == 1) {
@@ -304,7 +314,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t s_col = kColS + x * kBN, o_col = kColO + x * D;
         const float c = a.scale_log2;
         bool ok = true;
-        int step0 = 0;  // steps of this tile before the current block
+        int step0 = 0;     // steps of this tile before the current block
+        int uses = 0;      // uses of the staging buffer (by both tiles) before the current block
+        int blocks_x = 0;  // epilogues of this tile so far (phase of stage_full[x])
         for (int k = 0; ok && k * (int)gridDim.x < n_work; ++k) {
             const int Lw = persistent_work_index(k, n_work);
             if (Lw < 0) continue;
@@ -387,17 +399,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 warp_arrive(&p_full[x]);
             }
+            // the staging buffer's use number of this tile's epilogue in this block (tile A's before tile B's)
+            const int use = uses + (x == 1 && w.n_kv0 > 0);
+            uses += (w.n_kv0 > 0) + (w.n_kv1 > 0);
             if (!ok || n == 0) continue;
             // the block's last PV_X has completed: O_X is final
             step0 += n;
             ok = mbar_wait(&pv_done[x], (step0 - 1) & 1, a.status, kSiteFinal);
+            // the previous use's TMA store has finished reading the staging buffer
+            if (ok && use >= 1) ok = mbar_wait(stage_free, (use - 1) & 1, a.status, kSiteStage);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
             const float inv_l = 1.f / l;
-            // row stride and stored columns: the caller's D (at most this kernel's D; the columns past it
-            // hold zeros from the TMA's out-of-bounds fill)
-            const int Dr = a.D;
-            __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.o) + ((size_t)w.bh * N + row) * Dr;
+            // O / l as bf16 into the staging buffer: 128-byte-swizzled panels of 64 columns, row r of panel
+            // p at p * 16 KB + r * 128, its 16-byte chunk k at k ^ (r % 8) (conflict-free across the lanes)
             uint32_t ov[32];
 #pragma unroll
             for (int ch = 0; ch < D / 32; ++ch) {
@@ -408,21 +423,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_before();
                     warp_arrive(&o_free[x]);
                 }
-                if (row < N) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + ch * 32);
+                uint8_t *prow = stage + (ch >> 1) * (kBM * 128) + r * 128;
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4) {
-                        if (ch * 32 + v4 * 8 >= Dr) break;
-                        uint4 w4;
-                        w4.x = pack_bf16x2(__uint_as_float(ov[v4 * 8 + 0]) * inv_l, __uint_as_float(ov[v4 * 8 + 1]) * inv_l);
-                        w4.y = pack_bf16x2(__uint_as_float(ov[v4 * 8 + 2]) * inv_l, __uint_as_float(ov[v4 * 8 + 3]) * inv_l);
-                        w4.z = pack_bf16x2(__uint_as_float(ov[v4 * 8 + 4]) * inv_l, __uint_as_float(ov[v4 * 8 + 5]) * inv_l);
-                        w4.w = pack_bf16x2(__uint_as_float(ov[v4 * 8 + 6]) * inv_l, __uint_as_float(ov[v4 * 8 + 7]) * inv_l);
-                        dst[v4] = w4;
-                    }
+                for (int v4 = 0; v4 < 4; ++v4)
+                    st_shared_v4(prow + ((((ch & 1) * 4 + v4) ^ (r & 7)) << 4),
+                                 pack_bf16x2(__uint_as_float(ov[v4 * 8 + 0]) * inv_l, __uint_as_float(ov[v4 * 8 + 1]) * inv_l),
+                                 pack_bf16x2(__uint_as_float(ov[v4 * 8 + 2]) * inv_l, __uint_as_float(ov[v4 * 8 + 3]) * inv_l),
+                                 pack_bf16x2(__uint_as_float(ov[v4 * 8 + 4]) * inv_l, __uint_as_float(ov[v4 * 8 + 5]) * inv_l),
+                                 pack_bf16x2(__uint_as_float(ov[v4 * 8 + 6]) * inv_l, __uint_as_float(ov[v4 * 8 + 7]) * inv_l));
+            }
+            fence_proxy_async_smem();  // the staged tile is read by the TMA (async proxy)
+            warp_arrive(&stage_full[x]);
+            if (row < N) a.lse[(size_t)w.bh * N + row] = (m + __log2f(l)) * 0.69314718055994531f;
+            if (quarter == kFirstSoftmaxWarp % 4 && lane == 0) {
+                // one thread of the tile stores the staged panels (rows past N and columns past the caller's
+                // D are clipped by the tensor map) and frees the buffer once the stores have read it
+                if (mbar_wait(&stage_full[x], blocks_x & 1, a.status, kSiteStage)) {
+#pragma unroll
+                    for (int p = 0; p < kPanels; ++p)
+                        if (p * 64 < a.D) tma_store_3d(&tmap_o, stage + p * (kBM * 128), p * 64, tile_row0, w.bh);
+                    tma_store_commit();
+                    tma_store_wait_read();
+                    mbar_arrive(stage_free);
+                } else {
+                    ok = false;
                 }
             }
-            if (row < N) a.lse[(size_t)w.bh * N + row] = (m + __log2f(l)) * 0.69314718055994531f;
+            ++blocks_x;
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         }
     }
 
@@ -436,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, int NSLOT>
 cudaError_t launch_spec(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                        cudaStream_t s) {
+                        const CUtensorMap &to, cudaStream_t s) {
     using L = PairSmem<D, NSLOT>;
     static_assert(L::kAlloc <= 232448, "shared memory budget");
     auto kern = fwd_bf16_pair_kernel<D, NSLOT>;
@@ -445,16 +473,16 @@ cudaError_t launch_spec(const FwdArgs &a, const CUtensorMap &tq, const CUtensorM
     const int n_work = ((a.N + kTiles * kBM - 1) / (kTiles * kBM)) * a.H * a.B;
     const int sms = a.num_sms > 0 ? a.num_sms : kNumSms;
     dim3 grid(n_work < sms ? n_work : sms);
-    kern<<<grid, kThreads, L::kAlloc, s>>>(tq, tk, tv, a);
+    kern<<<grid, kThreads, L::kAlloc, s>>>(tq, tk, tv, to, a);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fwd_bf16_pair(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
-                                 const CUtensorMap &tv, cudaStream_t s) {
+                                 const CUtensorMap &tv, const CUtensorMap &to, cudaStream_t s) {
     switch (kernel_head_dim(a.D)) {
-        case 128: return launch_spec<128, 5>(a, tq, tk, tv, s);
+        case 128: return launch_spec<128, 4>(a, tq, tk, tv, to, s);
         default: return cudaErrorInvalidValue;
     }
 }
