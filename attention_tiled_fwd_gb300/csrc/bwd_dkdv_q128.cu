@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ int epi_abort;  // a compute warp's wait ran out: the epilogue stores nothing
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int rank, bh;
-    tile_order((a.N + kBN - 1) / kBN, a.B * a.H, a.causal, &rank, &bh);
+    tile_order((a.N + kBN - 1) / kBN, a.B * a.H, a.causal, a.head_group, &rank, &bh);
     const int k_tile = rank;  // causal: key tile 0 has the most query tiles
     const int N = a.N;
     const int n_q_total = (N + kBQ - 1) / kBQ;

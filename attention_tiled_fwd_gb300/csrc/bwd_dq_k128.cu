@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ int epi_abort;  // a compute warp's wait ran out: the epilogue stores nothing
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int rank, bh;
-    tile_order((a.N + kBM - 1) / kBM, a.B * a.H, a.causal, &rank, &bh);
+    tile_order((a.N + kBM - 1) / kBM, a.B * a.H, a.causal, a.head_group, &rank, &bh);
     const int q_tile = (a.N + kBM - 1) / kBM - 1 - rank;  // causal: the last query tile has the most keys
     const int N = a.N;
     const int kv_end = a.causal ? min(N, (q_tile + 1) * kBM) : N;

@@ -33,23 +33,36 @@ constexpr int kDqKRows = 64;    // dQ kernel: 128 query rows per CTA, 64-key K/V
 constexpr int kDkdvQRows = 64;  // dK/dV kernel: 128 keys per CTA, 64-query Q/dO tiles
 
 // Work order of a 1-D grid over (tile, batch*head).  Causal launches go by
-// tile rank across all heads, rank 0 (the most K/V tiles) first, so that the
-// hardware, which dispatches CTAs in index order, starts every SM on the
-// longest tiles and fills the tail with short ones.  Non-causal tiles are
-// equal, so the tiles of one head stay adjacent (they share its K/V in L2).
+// tile rank, rank 0 (the most K/V tiles) first, so that the hardware, which
+// dispatches CTAs in index order, starts every SM on the longest tiles and
+// fills the tail with short ones.  The ranks run across groups of `group`
+// heads, one group after the other, so that the K/V (or Q/dO) tiles that a
+// group's CTAs stream stay in L2 between the CTAs that read them; a group of
+// every head is the plain rank order.  Non-causal tiles are equal, so the
+// tiles of one head stay adjacent (they share its K/V in L2).
 #ifdef __CUDACC__
-__device__ __forceinline__ void tile_order_at(int L, int n_tiles, int n_bh, bool causal, int *rank, int *bh) {
-    if (causal) {
+__device__ __forceinline__ void tile_order_at(int L, int n_tiles, int n_bh, bool causal, int group, int *rank,
+                                              int *bh) {
+    if (causal && (group < 1 || group >= n_bh)) {
         *rank = L / n_bh;
         *bh = L % n_bh;
+    } else if (causal) {
+        const int g = group;
+        const int per = n_tiles * g;        // items of a full group
+        const int gi = L / per;             // L's group
+        const int g0 = gi * g;              // its first head
+        const int gs = min(g, n_bh - g0);   // its heads (the last group may have fewer)
+        const int in = L - gi * per;
+        *rank = in / gs;
+        *bh = g0 + in % gs;
     } else {
         *rank = L % n_tiles;
         *bh = L / n_tiles;
     }
 }
 
-__device__ __forceinline__ void tile_order(int n_tiles, int n_bh, bool causal, int *rank, int *bh) {
-    tile_order_at(blockIdx.x, n_tiles, n_bh, causal, rank, bh);
+__device__ __forceinline__ void tile_order(int n_tiles, int n_bh, bool causal, int group, int *rank, int *bh) {
+    tile_order_at(blockIdx.x, n_tiles, n_bh, causal, group, rank, bh);
 }
 
 // The k-th work item of CTA c in a persistent grid of G CTAs (one per SM): round k of the 1-D work
@@ -72,6 +85,11 @@ struct FwdArgs {
     int causal;
     int *status;       // device status word (bounded-wait failures)
     int num_sms;       // SMs of the device: the persistent forward runs one CTA per SM
+    int head_group;    // heads per group of the causal work order (tile_order_at)
+    // The persistent forwards' work counter (two ints, zero between launches: the next item to draw and
+    // the CTAs that have stopped drawing; the last of them zeroes both).  Null: the static deal
+    // persistent_work_index, used when the whole launch's K/V fits in L2.
+    int *work;
 };
 
 struct BwdArgs {
@@ -84,6 +102,7 @@ struct BwdArgs {
     int causal;
     int grad_bf16;  // 1: gradients stored as bf16, 0: fp32
     int *status;
+    int head_group;  // heads per group of the causal work order (tile_order_at)
 };
 
 // 5-GEMM comparator backward (bwd_atomic.cu): a.dq is the fp32 accumulator

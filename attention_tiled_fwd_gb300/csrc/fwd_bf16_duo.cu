@@ -23,6 +23,7 @@
 // after their last product that reads them (barriers of count 2); in a causal
 // block tile A has one K/V tile fewer and just commits for the last one.
 #include "fa_internal.h"
+#include "sched.cuh"
 #include "sm100_ptx.cuh"
 #include <cmath>
 
@@ -36,7 +37,7 @@ constexpr int kFirstSoftmaxWarp = 3;
 constexpr int kThreads = 32 * kFirstSoftmaxWarp + 128 * kTiles;
 
 enum : int { kSiteQ = 161, kSiteSlotEmpty, kSiteSlotFull, kSiteSFull, kSitePFull, kSitePV, kSiteFinal, kSiteDrain,
-             kSiteQEmpty, kSiteOFree, kSiteSFree };
+             kSiteQEmpty, kSiteOFree, kSiteSFree, kSiteWork };
 
 template <int D, int NSLOT>
 struct DuoSmem {
@@ -47,14 +48,16 @@ struct DuoSmem {
     static constexpr int kSlotOff = kTiles * kQBytes;
     static constexpr int kBarOff = kSlotOff + NSLOT * kSlotBytes;
     // q_full, q_empty, slot_full[NSLOT], slot_empty[NSLOT], per tile: s_full, p_full, pv_done, o_free, s_free,
-    // final
-    static constexpr int kNumBars = 2 + 2 * NSLOT + 5 * kTiles + kTiles;
+    // final; the work ring's full[kWorkRing], empty[kWorkRing]
+    static constexpr int kNumBars = 2 + 2 * NSLOT + 5 * kTiles + kTiles + 2 * kWorkRing;
     static constexpr int kTmemHolderOff = kBarOff + kNumBars * 8;
-    static constexpr int kAlloc = kTmemHolderOff + 16 + 1024;
+    static constexpr int kWorkOff = kTmemHolderOff + 16;  // the work ring's items
+    static constexpr int kAlloc = kWorkOff + 4 * kWorkRing + 1024;
 };
 
 // The work of one block of this CTA: which query rows, and how many K/V tiles each of its two query
-// tiles reads.  Every role of the CTA walks the same sequence of blocks and computes these alike.
+// tiles reads.  Every role of the CTA walks the same sequence of blocks (the work ring) and computes
+// these alike.
 struct DuoBlock {
     int bh, row0, n_kv0, n_kv1, n_all, n_q_tiles;
 };
@@ -62,7 +65,7 @@ struct DuoBlock {
 __device__ __forceinline__ DuoBlock duo_block(const FwdArgs &a, int L, int n_blk) {
     DuoBlock w;
     int rank;
-    tile_order_at(L, n_blk, a.B * a.H, a.causal, &rank, &w.bh);
+    tile_order_at(L, n_blk, a.B * a.H, a.causal, a.head_group, &rank, &w.bh);
     const int blk = n_blk - 1 - rank;  // causal: the last block has the most keys
     w.row0 = blk * (kTiles * kBM);
     auto tiles_of = [&](int x) -> int {
@@ -106,6 +109,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *o_free = pv_done + kTiles;    // [tile]: the epilogue has read O_X (phase = X's blocks with work)
     uint64_t *s_free = o_free + kTiles;     // [tile]: the softmax has loaded S_X of step g
     uint64_t *final_bar = s_free + kTiles;  // [tile]: every MMA of that tile's issuer has completed
+    // the blocks of this CTA, from the producer to the two issuers and the softmax warps (10 consumer warps)
+    const WorkRing ring{reinterpret_cast<int *>(smem + L::kWorkOff), final_bar + kTiles,
+                        final_bar + kTiles + kWorkRing};
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kTmemHolderOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -127,6 +133,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&o_free[x], 4);
             mbar_init(&s_free[x], 4);
             mbar_init(&final_bar[x], 1);
+        }
+        for (int i = 0; i < kWorkRing; ++i) {
+            mbar_init(&ring.full[i], 1);
+            mbar_init(&ring.empty[i], kTiles + 4 * kTiles);
         }
         fence_mbarrier_init();
     }
@@ -150,10 +160,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < NSLOT; ++s) last_round[s] = -1;
             int gidx = 0;  // K/V loads so far (ring position)
             int nb = 0;    // blocks so far
-            bool ok = true;
-            for (int k = 0; ok && k * (int)gridDim.x < n_work; ++k) {
-                const int Lw = persistent_work_index(k, n_work);
-                if (Lw < 0) continue;
+            int Lw = work_draw(a, 0, n_work);
+            bool ok = work_publish(ring, 0, Lw, a.status, kSiteWork);
+            while (ok && Lw >= 0) {
                 const DuoBlock w = duo_block(a, Lw, n_blk);
                 // Q of this block goes after its first K and V tiles: its buffer frees only when the
                 // previous block's last S products complete, and K_0 / V_0 need not wait for that
@@ -184,7 +193,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 gidx += 2 * w.n_all;
                 ++nb;
+                if (!ok) break;
+                // the next block, drawn once this one's loads are issued
+                Lw = work_draw(a, nb, n_work);
+                ok = work_publish(ring, nb, Lw, a.status, kSiteWork);
             }
+            work_finish(a);
             // Drain: never leave the CTA with a TMA write still in flight.
 #pragma unroll
             for (int s = 0; s < NSLOT; ++s)
@@ -214,9 +228,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (leader) mma_commit(bar);
             __syncwarp();
         };
-        for (int k = 0; ok && k * (int)gridDim.x < n_work; ++k) {
-            const int Lw = persistent_work_index(k, n_work);
-            if (Lw < 0) continue;
+        while (ok) {
+            const int Lw = work_take(ring, nb, a.status, kSiteWork, ok);
+            if (!ok || Lw < 0) break;
             const DuoBlock w = duo_block(a, Lw, n_blk);
             const int n = x == 0 ? w.n_kv0 : w.n_kv1;
             if (!(ok = warp_wait(q_full, nb & 1, a.status, kSiteQ))) break;
@@ -301,9 +315,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float c = a.scale_log2;
         bool ok = true;
         int step0 = 0;  // steps of this tile before the current block
-        for (int k = 0; ok && k * (int)gridDim.x < n_work; ++k) {
-            const int Lw = persistent_work_index(k, n_work);
-            if (Lw < 0) continue;
+        for (int k = 0; ok; ++k) {
+            const int Lw = work_take(ring, k, a.status, kSiteWork, ok);
+            if (!ok || Lw < 0) break;
             const DuoBlock w = duo_block(a, Lw, n_blk);
             const int n = x == 0 ? w.n_kv0 : w.n_kv1;
             const int tile_row0 = w.row0 + x * kBM;

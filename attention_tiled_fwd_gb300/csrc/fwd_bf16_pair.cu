@@ -32,6 +32,11 @@
 // so a block's Q load and first S products overlap the previous block's last
 // products and epilogue instead of a CTA exit, launch and pipeline fill
 // (measured +10 % at B=2 H=16 N=4096 D=128 causal, +5 % at N=32768 D=64).
+// Every role computes the CTA's blocks itself (the static deal), so the
+// causal order here is the plain rank order over all heads: blocks drawn from
+// a counter and handed to the issuer warp through shared memory (sched.cuh,
+// as the D = 64 kernel does) measured 10-15 % slower at D = 128, however the
+// hand-over was written.
 #include "fa_internal.h"
 #include "sm100_ptx.cuh"
 #include <cmath>
@@ -73,7 +78,7 @@ struct PairBlock {
 __device__ __forceinline__ PairBlock pair_block(const FwdArgs &a, int L, int n_blk) {
     PairBlock w;
     int rank;
-    tile_order_at(L, n_blk, a.B * a.H, a.causal, &rank, &w.bh);
+    tile_order_at(L, n_blk, a.B * a.H, a.causal, a.head_group, &rank, &w.bh);
     const int blk = n_blk - 1 - rank;  // causal: the last block has the most keys
     w.row0 = blk * (kTiles * kBM);
     auto tiles_of = [&](int x) -> int {

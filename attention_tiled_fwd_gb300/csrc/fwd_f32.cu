@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_f32_kernel(FwdArgs a) {
     float *v_s = k_s + kBN * (DP + 1);    // [kBN][DP]
 
     int rank, bh;
-    tile_order((a.N + kBM - 1) / kBM, a.B * a.H, a.causal, &rank, &bh);
+    tile_order((a.N + kBM - 1) / kBM, a.B * a.H, a.causal, a.head_group, &rank, &bh);
     const int q_tile = (a.N + kBM - 1) / kBM - 1 - rank;  // causal: the last query tile has the most keys
     const int N = a.N;
     const float *q = static_cast<const float *>(a.q) + (size_t)bh * N * D;

@@ -109,15 +109,18 @@ CSRC = "attention_tiled_fwd_gb300/csrc/"
 
 def kernel_sources(kernel: str, D: int, dtype: str = "bf16"):
     """The source files whose kernels run for `kernel` at head dimension D (for keying ncu figures)."""
-    common = [CSRC + "sm100_ptx.cuh", CSRC + "fa_internal.h"]
+    # fa_api.cu picks the causal work order (the head groups), which sets the DRAM traffic
+    common = [CSRC + "sm100_ptx.cuh", CSRC + "fa_internal.h", CSRC + "fa_api.cu"]
     if kernel == "fwd":
         if dtype == "f32":
             return [CSRC + "fwd_f32.cu", CSRC + "fa_internal.h"]
-        return [CSRC + "fwd_bf16.cu", CSRC + ("fwd_bf16_duo.cu" if D == 64 else "fwd_bf16_pair.cu")] + common
+        Dk = 64 if D <= 64 else 128 if D <= 128 else 256
+        own = {64: ["fwd_bf16_duo.cu", "sched.cuh"], 128: ["fwd_bf16_pair.cu"]}.get(Dk, [])
+        return [CSRC + "fwd_bf16.cu"] + [CSRC + f for f in own] + common
     if kernel == "bwd_dq":
-        return [CSRC + ("bwd_dq_k128.cu" if D == 64 else "bwd_dq.cu")] + common
+        return [CSRC + ("bwd_dq_k128.cu" if D <= 64 else "bwd_dq.cu")] + common
     if kernel == "bwd_dkdv":
-        return [CSRC + ("bwd_dkdv_q128.cu" if D == 64 else "bwd_dkdv.cu")] + common
+        return [CSRC + ("bwd_dkdv_q128.cu" if D <= 64 else "bwd_dkdv.cu")] + common
     return [CSRC + "bwd_atomic.cu"] + common
 
 
