@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // TMA producer (lane 0): K, V once, then Q_i, dO_i into the ring.  The whole warp: each query
-        // tile's L_i, D_i into the stats ring (lanes 0-15 four L values each, lanes 16-31 four D values).
+        // tile's L_i, D_i into the stats ring (4-byte copies, 32 consecutive words per instruction).
         if (lane == 0) {
             tma_prefetch_desc(&tmap_q);
             tma_prefetch_desc(&tmap_k);
@@ -217,15 +217,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             // stats of query tile i = idx / 2
             const int i = idx >> 1, ss = i % kStatSlots, sr = i / kStatSlots;
             if (!(ok = warp_wait(&stat_empty[ss], (sr & 1) ^ 1, a.status, kSiteStats))) break;
-            const bool is_l = lane < 16;
-            const int q = (q_begin + i) * kBQ + 4 * (lane & 15);
-            float *dst = stat_s + ss * 2 * kBQ + (is_l ? 0 : kBQ) + 4 * (lane & 15);
-            const float *src = is_l ? lse_g : del_g;
+            // lane l copies words l, l + 32, ... of the slot's [L_i | D_i]: each copy instruction writes 32
+            // consecutive words of shared memory (one bank each) from 32 consecutive floats
+            const int q0 = (q_begin + i) * kBQ;
+            float *dst = stat_s + ss * 2 * kBQ;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const bool valid = q + e < N;
-                asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst + e)),
-                             "l"(src + (valid ? q + e : 0)), "r"(valid ? 4 : 0)
+            for (int e = 0; e < 2 * kBQ / 32; ++e) {
+                const int w = 32 * e + lane;
+                const bool is_l = e < kBQ / 32;
+                const int q = q0 + (is_l ? w : w - kBQ);
+                const bool valid = q < N;
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst + w)),
+                             "l"((is_l ? lse_g : del_g) + (valid ? q : 0)), "r"(valid ? 4 : 0)
                              : "memory");
             }
             asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&stat_full[ss]))
