@@ -121,6 +121,8 @@ def kernel_sources(kernel: str, D: int, dtype: str = "bf16"):
         return [CSRC + ("bwd_dq_k128.cu" if D <= 64 else "bwd_dq.cu")] + common
     if kernel == "bwd_dkdv":
         return [CSRC + ("bwd_dkdv_q128.cu" if D <= 64 else "bwd_dkdv.cu")] + common
+    if kernel == "decode_stream":
+        return [CSRC + "decode.cu"] + common
     return [CSRC + "bwd_atomic.cu"] + common
 
 
@@ -438,9 +440,15 @@ def decode_main(args):
             "config": {"workload": "decode", **shape, "causal": True,
                        "l2": "flushed before every timed call (512 MB write), outside the timed events"},
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
-                         "traffic": None, "peak_source": f"{kind} hbm_gbs (copy)"},
+                         "traffic": traffic_for("decode_stream", decode_key(B, H, nq, N, D), D),
+                         "peak_source": f"{kind} hbm_gbs (copy)"},
             "gpu_launches": 2 * args.steps, "clocks": clocks}
     print(json.dumps(line), flush=True)
+
+
+def decode_key(B: int, H: int, n_q: int, N: int, D: int) -> str:
+    """The decode shape's key in the committed DRAM-traffic table."""
+    return f"decode_b{B}h{H}q{n_q}n{N}d{D}"
 
 
 # ----------------------------------------------------------------------------- every workload, one GPU
