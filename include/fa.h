@@ -26,6 +26,14 @@
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
  *     void*; NULL is the legacy default stream).  No entry point
  *     synchronises the host except fa_device_status().
+ *   - The library's own state is static device storage: the status word
+ *     below, the decode scratch of fa_decode_noalloc, and a ring of 1024
+ *     work counters that the D <= 64 causal forward draws its blocks from
+ *     when its keys and values exceed three quarters of L2 (each call takes
+ *     the next counter, and the launch zeroes it again when it ends).
+ *     Calls in flight at the same time on different streams therefore use
+ *     different counters; a captured CUDA graph keeps the counter it was
+ *     given, so one graph must not be replayed on two streams at once.
  *
  * Errors: every entry point returns FA_OK (0) or a negative fa_status.
  * Arguments are validated before anything is launched; on a validation
