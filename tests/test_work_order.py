@@ -4,8 +4,8 @@ A launch whose streamed operands exceed three quarters of L2 runs its causal til
 the D = 64 forward then draws its blocks from a per-launch counter that the launch zeroes again when it
 ends.  These tests take a shape that is grouped (B=1 H=24 N=16384 D=64 causal: 96 MiB of K and V) and
 check that every tile is computed (outputs prefilled with NaN come back finite), that sampled rows match
-the oracle, and that the counters leave nothing behind: repeated calls, and calls on two streams at
-once, give bit-identical results.
+the oracle, and that the counters leave nothing behind: repeated calls, calls on two streams at once,
+and replays of a captured CUDA graph give bit-identical results.
 """
 import numpy as np
 import pytest
@@ -98,3 +98,27 @@ def test_grouped_backward_covers_every_tile_and_matches_oracle():
     kidx = tuple(np.array(krows).T)
     assert_close(dk[kidx].double().cpu().numpy(), rdk, TOL_BF16, 0.0, what="grouped dK")
     assert_close(dv[kidx].double().cpu().numpy(), rdv, TOL_BF16, 0.0, what="grouped dV")
+
+
+def test_grouped_forward_in_a_cuda_graph_replays_identically():
+    """A captured launch keeps its work counter; every replay must find it zeroed by the one before."""
+    import attention_tiled_fwd_gb300 as fa
+    dev = cuda_or_skip()
+    _, d = _inputs(dev)
+    ref_o, ref_l = fa.fa_forward(d["q"], d["k"], d["v"], causal=True)
+    o, l = torch.empty_like(ref_o), torch.empty_like(ref_l)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fa.fa_forward(d["q"], d["k"], d["v"], causal=True, o=o, lse=l)  # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fa.fa_forward(d["q"], d["k"], d["v"], causal=True, o=o, lse=l)
+    for _ in range(3):
+        o.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert fa.fa_device_status() == 0
+        assert torch.equal(o, ref_o) and torch.equal(l, ref_l)
