@@ -22,10 +22,10 @@ struct FwdSpec {
     int D, BM, BN, nslot;
 };
 constexpr FwdSpec kFwdSpecs[] = {
-    {64, 256, 128, 10},  // Q 2 x 16 KB + 10 x 16 KB ring
-    {128, 256, 128, 5},  // Q 2 x 32 KB + 5 x 32 KB ring
-    {192, 128, 64, 7},  // Q 48 KB + 7 x 24 KB ring
-    {256, 128, 64, 4},  // Q 64 KB + 4 x 32 KB ring
+    {64, 256, 128, 4},   // Q 2 x 16 KB + 4 x 16 KB ring (6, 8, 10 slots measured 0-5 % slower; 5, 7, 9 more)
+    {128, 256, 128, 4},  // Q 2 x 32 KB + 4 x 32 KB ring + 32 KB staging for O's TMA stores
+    {192, 128, 64, 7},   // Q 48 KB + 7 x 24 KB ring (4, 5 slots measured 4-13 % slower)
+    {256, 128, 64, 4},   // Q 64 KB + 4 x 32 KB ring (3 slots measured 19 % slower)
 };
 
 // Tile rows of the backward kernels' streamed operands (TMA box heights).
@@ -176,6 +176,12 @@ cudaError_t launch_selftest_timeout(int *status, int limit_us, cudaStream_t s);
 // TMA loads a 64-column panel that reaches past D with zeros, which add nothing to a score or an
 // output column, and the kernels store only the D real columns (row stride D).
 inline int kernel_head_dim(int D) { return D <= 64 ? 64 : D <= 128 ? 128 : D <= 192 ? 192 : 256; }
+
+// K/V ring depth of the forward kernel of width D (a template argument of its launch).
+constexpr int fwd_nslot(int D) {
+    return D == 64 ? kFwdSpecs[0].nslot : D == 128 ? kFwdSpecs[1].nslot : D == 192 ? kFwdSpecs[2].nslot
+                                                                                     : kFwdSpecs[3].nslot;
+}
 
 inline int fwd_block_n(int D) {
     for (const auto &sp : kFwdSpecs)

@@ -410,8 +410,8 @@ cudaError_t launch_fwd_bf16(const FwdArgs &a, const CUtensorMap &tq, const CUten
         // issuer and a P buffer per tile (7 % faster there, 12-15 % slower at D = 128 without P buffers)
         case 64: return launch_fwd_bf16_duo(a, tq, tk, tv, s);
         case 128: return launch_fwd_bf16_pair(a, tq, tk, tv, to, s);
-        case 192: return launch_spec<192, 64, 7>(a, tq, tk, tv, s);
-        case 256: return launch_spec<256, 64, 4>(a, tq, tk, tv, s);
+        case 192: return launch_spec<192, 64, fwd_nslot(192)>(a, tq, tk, tv, s);
+        case 256: return launch_spec<256, 64, fwd_nslot(256)>(a, tq, tk, tv, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -473,7 +473,7 @@ cudaError_t launch_spec(const FwdArgs &a, const CUtensorMap &tq, const CUtensorM
 cudaError_t launch_fwd_bf16_duo(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
                                 const CUtensorMap &tv, cudaStream_t s) {
     switch (kernel_head_dim(a.D)) {
-        case 64: return launch_spec<64, 10>(a, tq, tk, tv, s);
+        case 64: return launch_spec<64, fwd_nslot(64)>(a, tq, tk, tv, s);
         default: return cudaErrorInvalidValue;
     }
 }

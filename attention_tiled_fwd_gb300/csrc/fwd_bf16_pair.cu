@@ -487,7 +487,7 @@ cudaError_t launch_spec(const FwdArgs &a, const CUtensorMap &tq, const CUtensorM
 cudaError_t launch_fwd_bf16_pair(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
                                  const CUtensorMap &tv, const CUtensorMap &to, cudaStream_t s) {
     switch (kernel_head_dim(a.D)) {
-        case 128: return launch_spec<128, 4>(a, tq, tk, tv, to, s);
+        case 128: return launch_spec<128, fwd_nslot(128)>(a, tq, tk, tv, to, s);
         default: return cudaErrorInvalidValue;
     }
 }
