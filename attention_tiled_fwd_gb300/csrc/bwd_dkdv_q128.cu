@@ -40,7 +40,7 @@ constexpr int kSpan = kBQ / kComputeWG;  // 32 queries per compute thread per ti
 constexpr int kFirstComputeWarp = 3;
 constexpr int kThreads = 32 * kFirstComputeWarp + 128 * kComputeWG;
 constexpr int kComputeWarps = 4 * kComputeWG;
-constexpr int kStatSlots = 4;     // query tiles' L / D in flight
+constexpr int kStatSlots = 2;     // query tiles' L / D in flight (1, 3 and 4 slots measured 1-36 % slower)
 constexpr int kNSlot = 10;        // Q_i / dO_i ring (5 tiles; 8 slots measured 1.6 % slower at N = 32768, 11 no better)
 
 enum : int { kSiteKV = 81, kSiteSlotEmpty, kSiteSlotFull, kSiteSFull, kSitePReady, kSiteDpFull, kSiteDsReady,
