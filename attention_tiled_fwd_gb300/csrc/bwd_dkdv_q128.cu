@@ -41,7 +41,7 @@ constexpr int kFirstComputeWarp = 3;
 constexpr int kThreads = 32 * kFirstComputeWarp + 128 * kComputeWG;
 constexpr int kComputeWarps = 4 * kComputeWG;
 constexpr int kStatSlots = 2;     // query tiles' L / D in flight (1, 3 and 4 slots measured 1-36 % slower)
-constexpr int kNSlot = 10;        // Q_i / dO_i ring (5 tiles; 8 slots measured 1.6 % slower at N = 32768, 11 no better)
+constexpr int kNSlot = 9;         // Q_i / dO_i ring (8 slots measured 0.3-1.8 % slower at N = 32768, 10 and 11 no faster)
 
 enum : int { kSiteKV = 81, kSiteSlotEmpty, kSiteSlotFull, kSiteSFull, kSitePReady, kSiteDpFull, kSiteDsReady,
              kSiteDone, kSiteFinal, kSiteDrain, kSiteStats, kSiteDkDone, kSiteDpFree };
