@@ -169,15 +169,15 @@ int current_num_sms() {
 
 // Heads per group of the causal work order (tile_order_at).  A launch streams two [N, D] bf16 operands per
 // head (K and V, or Q and dO); while those of every head fit in three quarters of L2 the order is the plain
-// rank order over all heads, otherwise a group holds as many heads as fit in half of it (at least one), so
-// that its operands stay in L2 while the group's CTAs read them.  (A quarter and an eighth of L2 measured
-// 1 % and 2 % slower at B=1 H=32 N=32768 D=64.)
+// rank order over all heads, otherwise a group holds as many heads as fit in a quarter of it (at least
+// one), so that its operands stay in L2 while the group's CTAs read them.  (Three eighths, a half, five
+// eighths and three quarters of L2 measured 0-3 % slower at B=1 H=32 N=32768 D=64 and N=16384 D=128.)
 int causal_head_group(const DeviceState &st, int B, int H, int N, int D) {
     const int n_bh = B * H;
     const double per_head = 4.0 * N * D;
     const double l2 = st.l2_bytes > 0 ? (double)st.l2_bytes : 126.0 * (1 << 20);
     if (per_head * n_bh <= 0.75 * l2) return n_bh;
-    return std::max(1, std::min(n_bh, (int)(0.5 * l2 / per_head)));
+    return std::max(1, std::min(n_bh, (int)(0.25 * l2 / per_head)));
 }
 
 // The persistent forwards draw their blocks from a work counter when the causal order runs by groups of
