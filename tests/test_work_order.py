@@ -2,7 +2,8 @@
 
 A launch whose streamed operands exceed three quarters of L2 runs its causal tiles by groups of heads;
 the D = 64 forward then draws its blocks from a per-launch counter that the launch zeroes again when it
-ends.  These tests take a shape that is grouped (B=1 H=24 N=16384 D=64 causal: 96 MiB of K and V) and
+ends.  These tests take a shape that is grouped (B=1 H=32 N=16384 D=64 causal: 128 MiB of K and V, more
+than three quarters of the 129 MB L2) and
 check that every tile is computed (outputs prefilled with NaN come back finite), that sampled rows match
 the oracle, and that the counters leave nothing behind: repeated calls, calls on two streams at once,
 and replays of a captured CUDA graph give bit-identical results.
@@ -17,7 +18,7 @@ from synthetic_inputs import make_qkv, sample_rows
 
 pytestmark = pytest.mark.gpu
 
-SHAPE = (1, 24, 16384, 64)
+SHAPE = (1, 32, 16384, 64)
 
 
 def _inputs(dev, with_dO=False):
