@@ -44,11 +44,14 @@
 // released after dQ_j, which is issued only after S_j completed.
 //
 // Wider heads (D = 192, 256) run the same kernel with two changes.  Q stays in
-// shared memory and S = Q K_j^T is an SS product, because dQ needs D (192) or
-// its share (128) of the 512 columns.  At D = 256, dQ alone would fill half of
-// TMEM, so two CTAs share each query tile: each computes S and dP over all D
-// (those products are repeated) and keeps one 128-column half of dQ (grid y =
-// the half).  At D = 192 one CTA keeps all 192 columns of dQ.
+// shared memory and S = Q K_j^T is an SS product, because dQ needs D of the 512
+// columns.  At D = 192 S and dP stay double-buffered beside dQ's 192 columns.
+// At D = 256 dQ takes 256 columns, so S and dP have one buffer each, which every
+// compute warp empties into registers first thing (s_free, dp_free) so that
+// S_{j+1} and dP_{j+1} can follow at once: TMEM S [0, 64), dP [64, 128), dQ
+// [128, 384), dS[b] [384 + 32b, +32).  (Two CTAs per query tile, each keeping
+// one half of dQ and both computing S and dP over all of D, measured 37-42 %
+// slower: the tensor core did 5/3 of the useful products.)
 #include "fa_internal.h"
 #include "sm100_ptx.cuh"
 #include <cmath>
@@ -63,7 +66,7 @@ constexpr int kFirstComputeWarp = 3;
 constexpr int kThreads = 32 * kFirstComputeWarp + 128 * kComputeWG;
 
 enum : int { kSiteQ = 21, kSiteSlotEmpty, kSiteSlotFull, kSiteSFull, kSiteDsFull, kSiteDq, kSiteFinal, kSiteDrain,
-             kSiteDqDone, kSiteQt };
+             kSiteDqDone, kSiteQt, kSiteSFree };
 
 template <int D, int NSLOT>
 struct DqSmem {
@@ -75,7 +78,7 @@ struct DqSmem {
     static constexpr int kOOff = kSlotOff + NSLOT * kTileBytes;
     // q_full, slot_full[NSLOT], slot_empty[NSLOT], s_full[2], ds_full[2], final, a_final, dq_done[2], qt_ready,
     // o_full, dp_full[2]
-    static constexpr int kNumBars = 1 + 2 * NSLOT + 12;
+    static constexpr int kNumBars = 1 + 2 * NSLOT + 14;
     static constexpr int kRest = kComputeWG * kBM * 4 + kNumBars * 8 + 16 + 1024;
     // O's tile is staged by TMA where it fits (D = 128): D_i is then summed from shared memory.  At larger D
     // the compute warps read the O and dO rows from global memory instead.
@@ -87,8 +90,8 @@ struct DqSmem {
 };
 
 // D: the contraction width the kernel is built for (64-column panels); DQ: the columns of dQ one
-// CTA accumulates (D, or D / 2 with grid y choosing the half); QT: Q kept in TMEM as the A operand of
-// S (else S reads Q from shared memory).
+// CTA accumulates (D here; D / DQ CTAs per query tile, grid y choosing the columns); QT: Q kept in
+// TMEM as the A operand of S (else S reads Q from shared memory).
 template <int D, int DQ, bool QT, int NSLOT>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -98,7 +101,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     using L = DqSmem<D, NSLOT>;
     constexpr int kPanels = D / 64;
     constexpr uint32_t kTmemCols = 512;
-    constexpr uint32_t kColDQ = 256, kColDS = 256 + DQ, kColQ = kColDS + 64;
+    // kSingle (D = 256 with all of dQ in one CTA): S and dP in one buffer each, emptied by the compute warps into
+    // registers first thing (s_free, dp_free), so that dQ's 256 columns fit beside them
+    constexpr bool kSingle = !QT && DQ == D && D == 256;
+    constexpr uint32_t kColDP0 = kSingle ? 64 : 128;  // dP[b] at kColDP0 + 64 b (b = 0 when kSingle)
+    constexpr uint32_t kColDQ = kSingle ? 128 : 256, kColDS = kColDQ + DQ, kColQ = kColDS + 64;
     static_assert(kColQ + (QT ? D / 2 : 0) <= 512, "TMEM budget");
     static_assert(DQ % 64 == 0 && D % DQ == 0, "dQ columns per CTA: whole panels");
     constexpr bool kSplitDp = !QT;
@@ -125,6 +132,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the dP product still executes, which measured 7-18 % faster there.  At D = 128 (Q in TMEM) s_full
     // covers S_j and dP_j both: the split measured 10 % slower.
     uint64_t *dp_full = o_full + 1;
+    uint64_t *s_free = dp_full + 2;  // kSingle: every compute warp has loaded S_j
+    uint64_t *dp_free = s_free + 1;  // kSingle: every compute warp has loaded dP_j
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kTmemHolderOff);
 
     __shared__ int epi_abort;  // a compute warp's wait ran out: the epilogue stores nothing
@@ -155,6 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = 0; b < 2; ++b) mbar_init(&dq_done[b], 1);
         mbar_init(qt_ready, 4 * kComputeWG);  // one arrive per compute warp
         mbar_init(o_full, 1);
+        mbar_init(s_free, 4 * kComputeWG);
+        mbar_init(dp_free, 4 * kComputeWG);
         fence_mbarrier_init();
     }
     if (warp == 1) {
@@ -223,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int v_slot = (2 * j + 1) % NSLOT, v_round = (2 * j + 1) / NSLOT;
             const uint32_t b = j & 1;
             // S[b], dP[b] last held tile j-2, which the compute warps have finished with
-            if (j >= 2 && !(ok = warp_wait(&ds_full[b], ((j - 2) >> 1) & 1, a.status, kSiteDsFull))) break;
+            if (!kSingle && j >= 2 && !(ok = warp_wait(&ds_full[b], ((j - 2) >> 1) & 1, a.status, kSiteDsFull))) break;
             if constexpr (!kSplitDp) {
                 if (!(ok = warp_wait(&slot_full[k_slot], k_round & 1, a.status, kSiteSlotFull))) break;
                 if (!(ok = warp_wait(&slot_full[v_slot], v_round & 1, a.status, kSiteSlotFull))) break;
@@ -245,25 +256,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
             } else {
                 if (!(ok = warp_wait(&slot_full[k_slot], k_round & 1, a.status, kSiteSlotFull))) break;
+                // kSingle: S_j overwrites S_{j-1}, which every compute warp must have loaded
+                if (kSingle && j >= 1 && !(ok = warp_wait(s_free, (j - 1) & 1, a.status, kSiteSFree))) break;
                 tc_fence_after();
+                const uint32_t sb = kSingle ? 0 : b;  // the S / dP buffer
                 const uint64_t k_desc = sdesc_sw128(slot_addr + k_slot * L::kTileBytes, 16, 1024);
                 const uint64_t v_desc = sdesc_sw128(slot_addr + v_slot * L::kTileBytes, 16, 1024);
                 if (leader) {
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks)
-                        mma_ss(tmem + 64 * b, sdesc_add(q_desc, (ks >> 2) * (kBM * 128) + (ks & 3) * 32),
+                        mma_ss(tmem + 64 * sb, sdesc_add(q_desc, (ks >> 2) * (kBM * 128) + (ks & 3) * 32),
                                sdesc_add(k_desc, (ks >> 2) * (kBN * 128) + (ks & 3) * 32), idesc_sq, ks > 0);
-                    mma_commit(&s_full[b]);
+                    mma_commit(&s_full[sb]);
                 }
                 __syncwarp();
                 if (!(ok = warp_wait(&slot_full[v_slot], v_round & 1, a.status, kSiteSlotFull))) break;
+                if (kSingle && j >= 1 && !(ok = warp_wait(dp_free, (j - 1) & 1, a.status, kSiteSFree))) break;
                 tc_fence_after();
                 if (leader) {
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks)
-                        mma_ss(tmem + 128 + 64 * b, sdesc_add(do_desc, (ks >> 2) * (kBM * 128) + (ks & 3) * 32),
+                        mma_ss(tmem + kColDP0 + 64 * sb, sdesc_add(do_desc, (ks >> 2) * (kBM * 128) + (ks & 3) * 32),
                                sdesc_add(v_desc, (ks >> 2) * (kBN * 128) + (ks & 3) * 32), idesc_sq, ks > 0);
-                    mma_commit(&dp_full[b]);
+                    mma_commit(&dp_full[sb]);
                     mma_commit(&slot_empty[v_slot]);  // V_j is no longer needed
                 }
                 __syncwarp();
@@ -398,7 +413,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
             const uint32_t b = j & 1;
-            ok = mbar_wait(&s_full[b], (j >> 1) & 1, a.status, kSiteSFull);
+            const uint32_t sb = kSingle ? 0 : b;                        // the S / dP buffer
+            const uint32_t sph = kSingle ? (j & 1) : ((j >> 1) & 1);   // its phase for tile j
+            ok = mbar_wait(&s_full[sb], sph, a.status, kSiteSFull);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
             const int key0 = j * kBN + g * kHalf;
@@ -432,8 +449,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 uint32_t sraw[kHalf], praw[kHalf];
                 uint64_t p2[kHalf / 2];
-                tmem_ld_n<kHalf>(tmem + lane_base + 64 * b + g * kHalf, sraw);
+                tmem_ld_n<kHalf>(tmem + lane_base + 64 * sb + g * kHalf, sraw);
                 tmem_wait_ld();
+                if constexpr (kSingle) {
+                    // S_j is in registers: S_{j+1} may overwrite the buffer
+                    tc_fence_before();
+                    warp_arrive(s_free);
+                }
                 // P = 2^(S c - L log2 e) while dP_j may still be executing, on fp32 pairs (f32x2)
 #pragma unroll
                 for (int i = 0; i < kHalf; i += 2) {
@@ -447,11 +469,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     p2[i / 2] = f2_pack(p0, p1);
                 }
-                ok = mbar_wait(&dp_full[b], (j >> 1) & 1, a.status, kSiteSFull);
+                ok = mbar_wait(&dp_full[sb], sph, a.status, kSiteSFull);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc_fence_after();
-                tmem_ld_n<kHalf>(tmem + lane_base + 128 + 64 * b + g * kHalf, praw);
+                tmem_ld_n<kHalf>(tmem + lane_base + kColDP0 + 64 * sb + g * kHalf, praw);
                 tmem_wait_ld();
+                if constexpr (kSingle) {
+                    tc_fence_before();
+                    warp_arrive(dp_free);
+                }
                 // dS / scale = P * (dP - D), two scores per instruction
 #pragma unroll
                 for (int i = 0; i < kHalf; i += 2)
@@ -549,7 +575,7 @@ cudaError_t launch_bwd_dq(const BwdArgs &a, const CUtensorMap &tq, const CUtenso
     switch (kernel_head_dim(a.D)) {
         case 128: return launch_spec<128, 128, true, 8>(a, tq, tk, tv, tdo, to, tdq, s);
         case 192: return launch_spec<192, 192, false, 4>(a, tq, tk, tv, tdo, to, tdq, s);  // 3, 5 slots slower
-        case 256: return launch_spec<256, 128, false, 3>(a, tq, tk, tv, tdo, to, tdq, s);
+        case 256: return launch_spec<256, 256, false, 3>(a, tq, tk, tv, tdo, to, tdq, s);
         default: return cudaErrorInvalidValue;
     }
 }
