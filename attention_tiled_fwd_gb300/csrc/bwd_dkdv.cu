@@ -48,9 +48,12 @@
 //
 // Wider heads run the same kernel.  At D = 192, dV and dK take 384 columns, so
 // S^T and dP^T are single-buffered (NB = 1): S^T_{i+1} waits for dV_i and dP^T_{i+1}
-// for dK_i.  At D = 256 two CTAs share each key tile (grid y = the half): each
-// computes S^T and dP^T over all D (those products are repeated) and keeps one
-// 128-column half of dV and dK, which leaves the D = 128 layout of TMEM.
+// for dK_i.  At D = 256 dV and dK (256 columns each) fill TMEM, so two CTAs share
+// each key tile and split the gradients (VK): the first keeps dV (S^T x 2 + dV),
+// the second dK (S^T x 2 + dP^T x 2 + dK); the dV CTA computes no dP^T, so the
+// tensor core does 5/4 of the useful products.  (Splitting the columns instead,
+// each CTA with half of dV and dK and both computing S^T and dP^T, did 6/4 and
+// measured 15 % slower.)
 #include "fa_internal.h"
 #include "sm100_ptx.cuh"
 #include <cmath>
@@ -84,9 +87,11 @@ struct DkdvSmem {
 };
 
 // D: the contraction width the kernel is built for (64-column panels); DO: the columns of dV and dK one
-// CTA accumulates (D, or D / 2 with grid y choosing the half); NB: S^T / dP^T buffers in TMEM (2, or 1
-// where dV and dK leave no room); kStatSlots: query tiles whose L / D are staged ahead.
-template <int D, int DO, int NB, int NSLOT, int kStatSlots>
+// CTA accumulates (D here); NB: S^T / dP^T buffers in TMEM (2, or 1 where dV and dK leave no room);
+// kStatSlots: query tiles whose L / D are staged ahead.
+// VK: the two CTAs of a key tile split the gradients rather than their columns (grid y = 0 keeps all of
+// dV, y = 1 all of dK); the dV CTA computes no dP^T, and neither repeats the other's product.
+template <int D, int DO, int NB, int NSLOT, int kStatSlots, bool VK>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
@@ -102,8 +107,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     static_assert(kSpan == 16 || kSpan == 32, "16 or 32 queries per compute thread");
     constexpr uint32_t kTmemCols = 512;
     // TMEM: S^T[b] = [64b, +64), dP^T[b] = [64 NB + 64b, +64), dV, dK (DO columns each)
-    constexpr uint32_t kColDP = 64 * NB, kColDV = 128 * NB, kColDK = 128 * NB + DO;
-    static_assert(128 * NB + 2 * DO <= 512, "TMEM budget");
+    // (VK: the CTA's one gradient at 128 NB)
+    constexpr uint32_t kColDP = 64 * NB, kColDV = 128 * NB, kColDK = VK ? 128 * NB : 128 * NB + DO;
+    static_assert(128 * NB + (VK ? 1 : 2) * DO <= 512, "TMEM budget");
     static_assert(DO % 64 == 0 && D % DO == 0 && (NB == 1 || NB == 2), "dV / dK columns per CTA: whole panels");
 
     extern __shared__ uint8_t smem_raw[];
@@ -140,7 +146,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_q_total = (N + kBQ - 1) / kBQ;
     const int q_begin = a.causal ? (k_tile * kBN) / kBQ : 0;
     const int n_q = n_q_total - q_begin;  // >= 1
-    const int do0 = blockIdx.y * DO;      // first dV / dK column of this CTA
+    const int do0 = VK ? 0 : blockIdx.y * DO;  // first dV / dK column of this CTA
+    const bool role_dv = VK && blockIdx.y == 0;  // VK: this CTA keeps dV only
+    const bool role_dk = VK && blockIdx.y == 1;  // VK: this CTA keeps dK only
     const int Dr = a.D;                   // row stride and real columns (<= D; the rest are zeros)
 
     if (threadIdx.x == 0) {
@@ -258,8 +266,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int d_slot = (2 * i + 1) % NSLOT, d_round = (2 * i + 1) / NSLOT;
             const uint32_t b = i % NB;
             if (!(ok = warp_wait(&slot_full[q_slot], q_round & 1, a.status, kSiteSlotFull))) break;
-            // buffer b last held P^T_{i-NB}, read by dV_{i-NB}
-            if (i >= NB && !(ok = warp_wait(&dv_done[b], ((i - NB) / NB) & 1, a.status, kSiteDvDone))) break;
+            // buffer b last held P^T_{i-NB}, read by dV_{i-NB} (the dK CTA: by the compute warps, done with
+            // tile i-NB once dK_{i-NB} was issued)
+            if (i >= NB && !(ok = warp_wait(role_dk ? &dk_done[b] : &dv_done[b], ((i - NB) / NB) & 1, a.status,
+                                            kSiteDvDone)))
+                break;
             tc_fence_after();
             const uint64_t q_desc = sdesc_sw128(slot_addr + q_slot * L::kTileBytes, 16, 1024);
             if (leader) {
@@ -270,6 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(&s_full[b]);
             }
             __syncwarp();
+            if (role_dv) continue;  // the dV CTA needs no dP^T
             if (!(ok = warp_wait(&slot_full[d_slot], d_round & 1, a.status, kSiteSlotFull))) break;
             // buffer b last held dS^T_{i-NB}, read by dK_{i-NB}
             if (i >= NB && !(ok = warp_wait(&dk_done[b], ((i - NB) / NB) & 1, a.status, kSiteDkDone))) break;
@@ -301,20 +313,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t p0 = (do0 / 64) * (kBQ * 128);
             const uint64_t qmn_desc = sdesc_sw128(slot_addr + q_slot * L::kTileBytes + p0, kBQ * 128, 1024);
             const uint64_t dmn_desc = sdesc_sw128(slot_addr + d_slot * L::kTileBytes + p0, kBQ * 128, 1024);
-            if (!(ok = warp_wait(&p_ready[b], (i / NB) & 1, a.status, kSitePReady))) break;
-            // p_ready only proves S^T_i, hence Q_i, complete: dO_i's copy may still be in flight when the
-            // ring is short, so wait for its slot too (normally long since done; the slot cannot refill
-            // before this warp's own release after dK_i, so the phase is never two behind)
-            if (!(ok = warp_wait(&slot_full[d_slot], ((2 * i + 1) / NSLOT) & 1, a.status, kSiteSlotFull))) break;
-            tc_fence_after();
-            if (leader) {
+            if (!role_dk) {
+                if (!(ok = warp_wait(&p_ready[b], (i / NB) & 1, a.status, kSitePReady))) break;
+                // p_ready only proves S^T_i, hence Q_i, complete: dO_i's copy may still be in flight when the
+                // ring is short, so wait for its slot too (normally long since done; the slot cannot refill
+                // before this warp's own release after dK_i, so the phase is never two behind)
+                if (!(ok = warp_wait(&slot_full[d_slot], ((2 * i + 1) / NSLOT) & 1, a.status, kSiteSlotFull)))
+                    break;
+                tc_fence_after();
+                if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < kBQ / 16; ++kk)
-                    mma_ts(tmem + kColDV, tmem + 64 * b + (kk / kStepsPerWG) * kSpan + (kk % kStepsPerWG) * 8,
-                           sdesc_add(dmn_desc, kk * 2048), idesc_g, (i > 0 || kk > 0));
-                mma_commit(&dv_done[b]);
+                    for (int kk = 0; kk < kBQ / 16; ++kk)
+                        mma_ts(tmem + kColDV, tmem + 64 * b + (kk / kStepsPerWG) * kSpan + (kk % kStepsPerWG) * 8,
+                               sdesc_add(dmn_desc, kk * 2048), idesc_g, (i > 0 || kk > 0));
+                    mma_commit(&dv_done[b]);
+                    if (role_dv) {
+                        // the dV CTA: S^T_i completed before P^T_i was produced, so after dV_i nothing reads
+                        // Q_i or dO_i any more
+                        mma_commit(&slot_empty[q_slot]);
+                        mma_commit(&slot_empty[d_slot]);
+                    }
+                }
+                __syncwarp();
+                if (role_dv) continue;
             }
-            __syncwarp();
             if (!(ok = warp_wait(&ds_ready[b], (i / NB) & 1, a.status, kSiteDsReady))) break;
             tc_fence_after();
             if (leader) {
@@ -398,6 +420,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_st();
             tc_fence_before();
             warp_arrive(&p_ready[b]);
+            if (role_dv) {  // the dV CTA computes no dS^T
+                warp_arrive(&stat_empty[ss]);
+                continue;
+            }
 
             ok = mbar_wait(&dp_full[b], (i / NB) & 1, a.status, kSiteDpFull);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -435,17 +461,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 128-byte-swizzled panels of 128 rows (64 bf16 or 32 fp32 columns; dV's panels first), and written
         // by TMA bulk stores that clip rows past N and columns past the caller's D.
         const int n_panels = a.grad_bf16 ? DO / 64 : DO / 32;  // per output
-        static_assert(2 * DO * 4 * kBN <= 2 * L::kKVBytes + NSLOT * L::kTileBytes, "staging fits");
+        static_assert((VK ? 1 : 2) * DO * 4 * kBN <= 2 * L::kKVBytes + NSLOT * L::kTileBytes, "staging fits");
         if (ok) {
             tc_fence_after();
             // the first half of the warpgroups writes dV, the second dK; each its share of the D columns
-            constexpr int kCols = DO / (kComputeWG / 2);
+            // (VK: every warpgroup writes its share of the CTA's one gradient, staged from offset 0)
+            constexpr int kCols = VK ? DO / kComputeWG : DO / (kComputeWG / 2);
             static_assert(kCols % 32 == 0, "32-column TMEM loads");
-            const bool is_dv = g < kComputeWG / 2;
-            const int c0 = (g % (kComputeWG / 2)) * kCols;
+            const bool is_dv = VK ? role_dv : g < kComputeWG / 2;
+            const int c0 = VK ? g * kCols : (g % (kComputeWG / 2)) * kCols;
             const uint32_t col = (is_dv ? kColDV : kColDK) + c0;
             const float osc = is_dv ? 1.f : sc;  // dK picks up the scale its dS^T operands left out
-            uint8_t *stage = smem + (is_dv ? 0 : n_panels) * (kBN * 128) + r * 128;
+            uint8_t *stage = smem + ((VK || is_dv) ? 0 : n_panels) * (kBN * 128) + r * 128;
             const int sw = r & 7;
             uint32_t v[32];
 #pragma unroll
@@ -481,8 +508,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int pw = a.grad_bf16 ? 64 : 32;  // panel width in elements
             for (int p = 0; p < n_panels; ++p) {
                 if (do0 + p * pw >= Dr) break;  // panels wholly past the caller's D are not stored
-                tma_store_3d(&tmap_dv, smem + p * (kBN * 128), do0 + p * pw, k_tile * kBN, bh);
-                tma_store_3d(&tmap_dk, smem + (n_panels + p) * (kBN * 128), do0 + p * pw, k_tile * kBN, bh);
+                if (!role_dk) tma_store_3d(&tmap_dv, smem + p * (kBN * 128), do0 + p * pw, k_tile * kBN, bh);
+                if (!VK) tma_store_3d(&tmap_dk, smem + (n_panels + p) * (kBN * 128), do0 + p * pw, k_tile * kBN, bh);
+                if (role_dk) tma_store_3d(&tmap_dk, smem + p * (kBN * 128), do0 + p * pw, k_tile * kBN, bh);
             }
             tma_store_commit();
             tma_store_wait_read();  // the CTA's shared memory must outlive the stores' reads
@@ -497,15 +525,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D, int DO, int NB, int NSLOT, int STATS>
+template <int D, int DO, int NB, int NSLOT, int STATS, bool VK = false>
 cudaError_t launch_spec(const BwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                         const CUtensorMap &tdo, const CUtensorMap &tdk, const CUtensorMap &tdv, cudaStream_t s) {
     using L = DkdvSmem<D, NSLOT, STATS>;
     static_assert(L::kAlloc <= 232448, "shared memory budget");
-    auto kern = bwd_dkdv_kernel<D, DO, NB, NSLOT, STATS>;
+    auto kern = bwd_dkdv_kernel<D, DO, NB, NSLOT, STATS, VK>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
-    dim3 grid(((a.N + kBN - 1) / kBN) * a.H * a.B, D / DO);
+    dim3 grid(((a.N + kBN - 1) / kBN) * a.H * a.B, VK ? 2 : D / DO);
     kern<<<grid, kThreads, L::kAlloc, s>>>(tq, tk, tv, tdo, tdk, tdv, a);
     return cudaGetLastError();
 }
@@ -517,7 +545,7 @@ cudaError_t launch_bwd_dkdv(const BwdArgs &a, const CUtensorMap &tq, const CUten
     switch (kernel_head_dim(a.D)) {
         case 128: return launch_spec<128, 128, 2, 8, 4>(a, tq, tk, tv, tdo, tdk, tdv, s);
         case 192: return launch_spec<192, 192, 1, 5, 4>(a, tq, tk, tv, tdo, tdk, tdv, s);
-        case 256: return launch_spec<256, 128, 2, 3, 3>(a, tq, tk, tv, tdo, tdk, tdv, s);
+        case 256: return launch_spec<256, 256, 2, 3, 3, true>(a, tq, tk, tv, tdo, tdk, tdv, s);
         default: return cudaErrorInvalidValue;
     }
 }
