@@ -17,7 +17,7 @@
 
 namespace fa {
 
-constexpr int kWorkRing = 4;  // items in flight between the producer and the consumer warps
+constexpr int kWorkRing = 2;  // items in flight between the producer and the consumer warps (4, 8 no faster)
 
 struct WorkRing {
     int *item;        // [kWorkRing] in shared memory
